@@ -1,0 +1,206 @@
+/*
+ * dustin.h -- C-ABI of the GB300 (sm_103a) library for Dustin's
+ * draft-augmented sparse verification hot path.
+ *
+ * Sources of the operations (cited by page title and section):
+ *   [Paper]  "Dustin: Draft-Augmented Sparse Verification for Efficient
+ *            Long-Context Generation with Speculative Decoding"
+ *            (arXiv 2606.24957, HTML translation), section 3.1 Eq. (1)-(4).
+ *   [Notes]  "dustin-long-context" paper notes: section 2.2 (S_Draft,
+ *            S_Target, one global index set, Fig. 5), section 2.3
+ *            (I_verify = sink + window + draft top-m + target rest),
+ *            section 2.4 (SRH: scoring on a few (layer, head) pairs, Fig. 6),
+ *            section 3 (Fig. 7 self-attention speedup against full cache).
+ *
+ * Conventions shared by every call:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the
+ *     library keeps no reference after the call returns and allocates
+ *     no device memory.  Scratch space, where a call needs it, is passed by
+ *     the caller as (ws, ws_bytes), sized by the matching *_workspace_size
+ *     query for the current device.
+ *   - bf16 tensors are IEEE bfloat16 bit patterns (uint16), row-major, with
+ *     the innermost (head-dim) axis contiguous.  Base pointers and row
+ *     strides must be 16-byte aligned.
+ *   - Every compute call is asynchronous on `stream` (a cudaStream_t; NULL
+ *     is the legacy default stream) and returns a dustin_status.  Arguments
+ *     are validated on the host before anything is launched: an invalid call
+ *     launches nothing.  A failed launch returns DUSTIN_ERR_CUDA with the
+ *     CUDA error text in dustin_last_error().  Nothing is thrown across the
+ *     ABI and no kernel traps.
+ *   - Device-side checks (an index >= n, a page id outside the pool) never
+ *     fault: the offending position is left out of the attention and a flag
+ *     is raised, read with dustin_device_status().
+ *   - Grouped-query attention: query head h reads kv head h / (h_q / h_kv).
+ */
+#ifndef DUSTIN_H_
+#define DUSTIN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum dustin_status {
+  DUSTIN_OK = 0,
+  DUSTIN_ERR_INVALID_ARG = 1, /* NULL pointer where one is needed, bad enum */
+  DUSTIN_ERR_SHAPE = 2,       /* sizes inconsistent or out of range         */
+  DUSTIN_ERR_UNSUPPORTED = 3, /* valid but not built (e.g. d not 64 / 128)  */
+  DUSTIN_ERR_WORKSPACE = 4,   /* workspace NULL or smaller than required    */
+  DUSTIN_ERR_ALIGNMENT = 5,   /* pointer or stride not 16-byte aligned      */
+  DUSTIN_ERR_CUDA = 6,        /* a CUDA runtime call failed                 */
+  DUSTIN_ERR_DEVICE = 7       /* a device-side check raised a flag          */
+} dustin_status;
+
+/* Device-side flags reported by dustin_device_status(). */
+#define DUSTIN_DEVFLAG_INDEX_RANGE 0x1u /* idx[b][i] < 0 or >= n            */
+#define DUSTIN_DEVFLAG_PAGE_RANGE 0x2u  /* page id < 0 or >= num_pages      */
+
+#define DUSTIN_NORM_NONE 0 /* hybrid mix of the raw score vectors          */
+#define DUSTIN_NORM_L1 1   /* each score vector divided by its own sum     */
+
+/*
+ * One layer's KV cache for one (layer) of the target or the draft.
+ *
+ * Contiguous layout (page_table == NULL): element (b, kv head h, position
+ * j, dim c) is at  base + b*stride_b + h*stride_h + j*stride_n + c.
+ * Paged layout (page_table != NULL): a pool of pages [page][h_kv][page_size]
+ * [d]; position j of sequence b lives in page
+ * p = page_table[b*pages_per_seq + j/page_size] at
+ * base + p*stride_b + h*stride_h + (j % page_size)*stride_n + c, so stride_b
+ * is then the stride between pages.  page_table is a device int32 array.
+ * v may be NULL for calls that read keys only (scoring).
+ * Strides are in elements; every stride must be a multiple of 8 (16 bytes).
+ */
+typedef struct dustin_kv {
+  const void* k;
+  const void* v;
+  int64_t stride_b;
+  int64_t stride_h;
+  int64_t stride_n;
+  const int32_t* page_table;
+  int32_t page_size;
+  int32_t pages_per_seq;
+  int32_t num_pages;
+} dustin_kv;
+
+/* Text for a status code (static storage, never NULL). */
+const char* dustin_status_string(int status);
+
+/* Detail of the last failing call on this host thread ("" if none). */
+const char* dustin_last_error(void);
+
+/* Library ABI version: major*10000 + minor*100 + patch. */
+int dustin_version(void);
+
+/* Number of kernels this library has launched in this process. */
+uint64_t dustin_launch_count(void);
+
+/*
+ * Reads and clears the device-side flags (DUSTIN_DEVFLAG_*) of the current
+ * device.  Synchronises the device.  Returns DUSTIN_ERR_DEVICE if any flag
+ * was set, DUSTIN_OK otherwise; *flags (may be NULL) receives the flags.
+ */
+int dustin_device_status(uint32_t* flags);
+
+/* ------------------------------------------------------------------------
+ * Importance scoring on the scored (layer, head) pairs.
+ *
+ * [Notes] section 2.2: S_Draft sums the draft's attention over its heads,
+ * layers and Gamma lookahead queries; S_Target sums the target's attention
+ * of its latest token over its heads and layers.  [Notes] section 2.4
+ * (Fig. 6): only the selected (layer, head) pairs are recomputed.
+ *
+ *   s_out[b][j] = sum_{p < n_pairs} sum_{r < rows}
+ *                 softmax_j( scale * q[p][b][r] . K_p[b][kv_head[p]][j] )
+ * over history positions j in [0, n); fp32 out, fp32 accumulation.
+ *
+ *   q        bf16 [n_pairs][b][rows][d], device
+ *   kv       host array [n_pairs]: the key cache of pair p's layer (v unused)
+ *   kv_head  host array [n_pairs]: kv head of pair p (q_head / group)
+ *   s_out    fp32 [b][n], device, fully overwritten
+ *   ws       device scratch of dustin_score_heads_workspace_size() bytes
+ * Called once for the target (rows = 1) and once for the draft
+ * (rows = Gamma).  Limits: d in {64, 128}; 1 <= rows <= 16;
+ * 1 <= n_pairs <= 64; n_pairs * rows <= 1024.
+ * b == 0 or n == 0 is a no-op.
+ */
+size_t dustin_score_heads_workspace_size(int b, int n, int n_pairs, int rows);
+int dustin_score_heads(int b, int n, int d, int n_pairs, int rows,
+                       const void* q, const dustin_kv* kv,
+                       const int32_t* kv_head, float scale, float* s_out,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Hybrid combination and global per-sequence Top-K ([Notes] sections 2.2
+ * and 2.3).  One index set per sequence, shared by all layers and heads.
+ *
+ * Protected positions [0, n_sink) and [n - n_recent, n) are always kept;
+ * k counts them.  The remaining budget r = k - |protected| is filled from
+ * the other positions:
+ *   m < 0  (alpha mode): top-r of c_j = a_D*S_D[j] + a_T*S_T[j], where
+ *          a_D = alpha / sum(S_D) and a_T = (1 - alpha) / sum(S_T) under
+ *          DUSTIN_NORM_L1 (alpha and 1 - alpha under DUSTIN_NORM_NONE).
+ *          Sums in fp64, coefficients rounded once to fp32, then
+ *          c_j = fl(fl(a_D*S_D[j]) + fl(a_T*S_T[j])) in fp32 round-to-nearest.
+ *          A term with weight 0 or a NULL vector is left out.  A sum that is
+ *          not positive and finite leaves that vector unscaled.
+ *   m >= 0 (budget split): top-min(m, r) of S_D, then the top of S_T for the
+ *          rest of the budget over the positions not yet taken.
+ * Order: higher score first, ties to the lower position; -0 equals +0; NaN
+ * ranks below every number.  idx rows come out strictly ascending.
+ * k >= n keeps all n positions (idx row length n).
+ *
+ *   s_draft, s_target  fp32 [b][n], device; either may be NULL (not both)
+ *   idx                int32 [b][min(k, n)], device, fully overwritten
+ * Errors: |protected| > k with k < n is DUSTIN_ERR_SHAPE.  n <= 2^20.
+ */
+int dustin_hybrid_topk(int b, int n, int k, int n_sink, int n_recent,
+                       double alpha, int m, int norm, const float* s_draft,
+                       const float* s_target, int32_t* idx, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Sparse verification attention ([Notes] section 2.2 Fig. 5, Stage 2: the
+ * target verifies its w window rows over the selected KV only).
+ *
+ * For each sequence b, query head h and window row t (no causal mask: all
+ * selected history precedes the window; the window's own causal block is
+ * merged by the caller through lse):
+ *   o[b][h][t]   = softmax_i(scale * q[b][h][t] . K[b][g][idx[b][i]]) V[..]
+ *   lse[b][h][t] = log sum_i exp(scale * q[b][h][t] . K[b][g][idx[b][i]])
+ * with g = h / (h_q / h_kv).  k == 0 gives o = 0, lse = -inf.
+ *
+ *   q    bf16 [b][h_q][w][d], device (contiguous)
+ *   kv   host pointer to one dustin_kv (k and v both required)
+ *   idx  int32 [b][k], device, each entry in [0, n); ascending order is
+ *        fastest but not required
+ *   o    bf16 [b][h_q][w][d], device;  lse fp32 [b][h_q][w] (natural log)
+ *   ws   device scratch of dustin_sparse_verify_attn_workspace_size() bytes
+ *        (may be 0 bytes; ws may then be NULL)
+ * Limits: d in {64, 128}; h_q a multiple of h_kv; k <= n.
+ */
+size_t dustin_sparse_verify_attn_workspace_size(int b, int h_q, int h_kv,
+                                                int d, int w, int k);
+int dustin_sparse_verify_attn(int b, int h_q, int h_kv, int d, int w, int n,
+                              int k, const void* q, const dustin_kv* kv,
+                              const int32_t* idx, float scale, void* o,
+                              float* lse, void* ws, size_t ws_bytes,
+                              void* stream);
+
+/* ------------------------------------------------------------------------
+ * Full-cache verification attention: the dense in-run baseline ([Notes]
+ * section 3, Fig. 7 "Full Cache").  The sparse call over idx = 0..n-1.
+ */
+size_t dustin_full_verify_attn_workspace_size(int b, int h_q, int h_kv,
+                                              int d, int w, int n);
+int dustin_full_verify_attn(int b, int h_q, int h_kv, int d, int w, int n,
+                            const void* q, const dustin_kv* kv, float scale,
+                            void* o, float* lse, void* ws, size_t ws_bytes,
+                            void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DUSTIN_H_ */

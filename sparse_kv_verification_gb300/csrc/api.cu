@@ -1,0 +1,411 @@
+// C-ABI of the Dustin sparse-verification library (declared in
+// include/dustin.h): host-side validation, launch planning and dispatch.
+// Nothing here allocates device memory; scratch comes from the caller.
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "attn.cuh"
+#include "dustin.h"
+#include "internal.h"
+
+namespace dustin {
+
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+thread_local char g_err[512] = "";
+
+int fail(int status, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return status;
+}
+
+int cuda_fail(cudaError_t e, const char* where) {
+  return fail(DUSTIN_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+      cudaSuccess)
+    return 1;
+  return sms > 0 ? sms : 1;
+}
+
+KvView to_view(const dustin_kv& kv) {
+  KvView v;
+  v.k = static_cast<const __nv_bfloat16*>(kv.k);
+  v.v = static_cast<const __nv_bfloat16*>(kv.v);
+  v.sb = kv.stride_b;
+  v.sh = kv.stride_h;
+  v.sn = kv.stride_n;
+  v.page_table = kv.page_table;
+  v.page_size = kv.page_size;
+  v.pages_per_seq = kv.pages_per_seq;
+  v.num_pages = kv.num_pages;
+  return v;
+}
+
+// Checks a KV descriptor for `b` sequences of `n` positions with head dim d.
+int check_kv(const dustin_kv* kv, int b, int n, int d, bool need_v,
+             const char* what) {
+  if (!kv) return fail(DUSTIN_ERR_INVALID_ARG, "%s: kv is NULL", what);
+  if (!kv->k) return fail(DUSTIN_ERR_INVALID_ARG, "%s: kv.k is NULL", what);
+  if (need_v && !kv->v)
+    return fail(DUSTIN_ERR_INVALID_ARG, "%s: kv.v is NULL", what);
+  if (!aligned16(kv->k) || (need_v && !aligned16(kv->v)))
+    return fail(DUSTIN_ERR_ALIGNMENT, "%s: kv base not 16-byte aligned", what);
+  if (kv->stride_b < 0 || kv->stride_h < 0 || kv->stride_n < d)
+    return fail(DUSTIN_ERR_SHAPE, "%s: bad kv strides (%lld, %lld, %lld)", what,
+                (long long)kv->stride_b, (long long)kv->stride_h,
+                (long long)kv->stride_n);
+  if (kv->stride_b % 8 || kv->stride_h % 8 || kv->stride_n % 8)
+    return fail(DUSTIN_ERR_ALIGNMENT,
+                "%s: kv strides must be multiples of 8 elements", what);
+  if (kv->page_table) {
+    if (kv->page_size < 16 || kv->page_size % 16)
+      return fail(DUSTIN_ERR_UNSUPPORTED,
+                  "%s: page_size %d (must be a positive multiple of 16)", what,
+                  kv->page_size);
+    if (kv->num_pages < 1)
+      return fail(DUSTIN_ERR_SHAPE, "%s: num_pages %d", what, kv->num_pages);
+    const long long need = ((long long)n + kv->page_size - 1) / kv->page_size;
+    if (kv->pages_per_seq < need)
+      return fail(DUSTIN_ERR_SHAPE, "%s: pages_per_seq %d < %lld", what,
+                  kv->pages_per_seq, need);
+    if ((reinterpret_cast<uintptr_t>(kv->page_table) & 3u) != 0)
+      return fail(DUSTIN_ERR_ALIGNMENT, "%s: page_table misaligned", what);
+  }
+  (void)b;
+  return DUSTIN_OK;
+}
+
+// ---- attention planning
+struct AttnPlan {
+  int mt, row_blocks, splits, chunk;
+  size_t ws_o, ws_ml;
+};
+
+AttnPlan plan_attn(bool dense, int b, int hq, int hkv, int d, int w, int npos) {
+  AttnPlan p;
+  const int group = hq / hkv;
+  const long long rows = (long long)group * w;
+  p.mt = (int)std::min<long long>(4, (rows + 15) / 16);
+  if (p.mt < 1) p.mt = 1;
+  p.row_blocks = (int)((rows + 16 * p.mt - 1) / (16 * p.mt));
+  const long long units = (long long)b * hkv * p.row_blocks;
+  const int tiles = (npos + 63) / 64;
+  if (tiles == 0 || units == 0) {
+    p.splits = 1;
+    p.chunk = 64;
+  } else {
+    const int occ = dense ? occupancy_attn_dense(d, p.mt)
+                          : occupancy_attn_sparse(d, p.mt);
+    const long long slots = (long long)sm_count() * occ;
+    long long s = units >= slots ? 1 : slots / units;
+    s = std::min<long long>(s, tiles);
+    long long ct = (tiles + s - 1) / s;
+    // Offset-table cap: 2048 rows (sparse) or 2047 pages of >= 16 (dense).
+    const long long cap = dense ? (2047LL * 16) / 64 : 2048 / 64;
+    ct = std::min(ct, cap);
+    p.splits = (int)((tiles + ct - 1) / ct);
+    p.chunk = (int)(ct * 64);
+  }
+  if (p.splits > 1) {
+    const size_t prows = (size_t)units * p.splits * 16 * p.mt;
+    p.ws_o = align256(prows * d * sizeof(float));
+    p.ws_ml = align256(prows * sizeof(float2));
+  } else {
+    p.ws_o = p.ws_ml = 0;
+  }
+  return p;
+}
+
+int check_attn_shape(int b, int hq, int hkv, int d, int w, int n,
+                     const char* what) {
+  if (b < 0 || n < 0 || w < 1 || hq < 1 || hkv < 1)
+    return fail(DUSTIN_ERR_SHAPE, "%s: b=%d n=%d w=%d h_q=%d h_kv=%d", what, b,
+                n, w, hq, hkv);
+  if (hq % hkv)
+    return fail(DUSTIN_ERR_SHAPE, "%s: h_q %d not a multiple of h_kv %d", what,
+                hq, hkv);
+  if (d != 64 && d != 128)
+    return fail(DUSTIN_ERR_UNSUPPORTED, "%s: d=%d (64 or 128)", what, d);
+  const long long blocks = (long long)b * hkv *
+                           (((long long)(hq / hkv) * w + 63) / 64);
+  if (blocks > (1LL << 24))
+    return fail(DUSTIN_ERR_SHAPE, "%s: problem too large", what);
+  return DUSTIN_OK;
+}
+
+int run_attn(bool dense, int b, int hq, int hkv, int d, int w, int n, int k,
+             const void* q, const dustin_kv* kv, const int32_t* idx,
+             float scale, void* o, float* lse, void* ws, size_t ws_bytes,
+             void* stream) {
+  const char* what = dense ? "dustin_full_verify_attn" : "dustin_sparse_verify_attn";
+  int rc = check_attn_shape(b, hq, hkv, d, w, n, what);
+  if (rc) return rc;
+  if (!dense && (k < 0 || k > n))
+    return fail(DUSTIN_ERR_SHAPE, "%s: k=%d must be in [0, n=%d]", what, k, n);
+  if (b == 0) return DUSTIN_OK;
+  if (!q || !o || !lse)
+    return fail(DUSTIN_ERR_INVALID_ARG, "%s: q, o and lse are required", what);
+  if (!dense && k > 0 && !idx)
+    return fail(DUSTIN_ERR_INVALID_ARG, "%s: idx is NULL", what);
+  if (!aligned16(q) || !aligned16(o) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u) ||
+      (idx && (reinterpret_cast<uintptr_t>(idx) & 3u)))
+    return fail(DUSTIN_ERR_ALIGNMENT, "%s: q/o need 16-byte, lse/idx 4-byte alignment",
+                what);
+  if (!std::isfinite(scale))
+    return fail(DUSTIN_ERR_INVALID_ARG, "%s: scale is not finite", what);
+  rc = check_kv(kv, b, n, d, true, what);
+  if (rc) return rc;
+  const int npos = dense ? n : k;
+  AttnPlan p = plan_attn(dense, b, hq, hkv, d, w, npos);
+  if ((long long)b * hkv * p.row_blocks * p.splits > 0x7fffffffLL)
+    return fail(DUSTIN_ERR_SHAPE, "%s: grid too large", what);
+  const size_t need = p.ws_o + p.ws_ml;
+  if (need > 0 && (!ws || ws_bytes < need || !aligned16(ws)))
+    return fail(DUSTIN_ERR_WORKSPACE, "%s: workspace %zu bytes, need %zu (16-byte aligned)",
+                what, ws_bytes, need);
+  AttnArgs a;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.lse = lse;
+  a.kv = to_view(*kv);
+  a.idx = dense ? nullptr : idx;
+  a.b = b;
+  a.hq = hq;
+  a.hkv = hkv;
+  a.w = w;
+  a.n = n;
+  a.npos = npos;
+  a.group = hq / hkv;
+  a.rows = a.group * w;
+  a.row_blocks = p.row_blocks;
+  a.splits = p.splits;
+  a.chunk = p.chunk;
+  a.scale_log2 = scale * kLog2e;
+  a.ws_o = need ? static_cast<float*>(ws) : nullptr;
+  a.ws_ml = need ? reinterpret_cast<float2*>(static_cast<char*>(ws) + p.ws_o)
+                 : nullptr;
+  const bool paged = kv->page_table != nullptr;
+  cudaError_t e = dense ? launch_attn_dense(a, d, p.mt, paged, (cudaStream_t)stream)
+                        : launch_attn_sparse(a, d, p.mt, paged, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  return DUSTIN_OK;
+}
+
+}  // namespace
+
+void note_launches(int count) { g_launches.fetch_add((uint64_t)count); }
+
+}  // namespace dustin
+
+using namespace dustin;
+
+extern "C" {
+
+const char* dustin_status_string(int status) {
+  switch (status) {
+    case DUSTIN_OK: return "ok";
+    case DUSTIN_ERR_INVALID_ARG: return "invalid argument";
+    case DUSTIN_ERR_SHAPE: return "bad shape";
+    case DUSTIN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case DUSTIN_ERR_WORKSPACE: return "workspace missing or too small";
+    case DUSTIN_ERR_ALIGNMENT: return "misaligned pointer or stride";
+    case DUSTIN_ERR_CUDA: return "CUDA error";
+    case DUSTIN_ERR_DEVICE: return "device-side check failed";
+    default: return "unknown status";
+  }
+}
+
+const char* dustin_last_error(void) { return g_err; }
+
+int dustin_version(void) { return 100; }
+
+uint64_t dustin_launch_count(void) { return g_launches.load(); }
+
+int dustin_device_status(uint32_t* flags) {
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "dustin_device_status");
+  unsigned f = 0;
+  if ((e = take_attn_sparse_flags(&f)) != cudaSuccess ||
+      (e = take_attn_dense_flags(&f)) != cudaSuccess ||
+      (e = take_score_flags(&f)) != cudaSuccess)
+    return cuda_fail(e, "dustin_device_status");
+  if (flags) *flags = f;
+  if (f) return fail(DUSTIN_ERR_DEVICE, "device flags 0x%x", f);
+  return DUSTIN_OK;
+}
+
+size_t dustin_score_heads_workspace_size(int b, int n, int n_pairs, int rows) {
+  if (b <= 0 || n <= 0 || n_pairs <= 0 || rows <= 0) return 0;
+  const long long chunk = score_chunk();
+  const long long nch = (n + chunk - 1) / chunk;
+  const size_t prs = (size_t)n_pairs * rows * b;
+  return align256(prs * n * sizeof(float)) + align256(prs * nch * sizeof(float2));
+}
+
+int dustin_score_heads(int b, int n, int d, int n_pairs, int rows,
+                       const void* q, const dustin_kv* kv,
+                       const int32_t* kv_head, float scale, float* s_out,
+                       void* ws, size_t ws_bytes, void* stream) {
+  const char* what = "dustin_score_heads";
+  if (b < 0 || n < 0) return fail(DUSTIN_ERR_SHAPE, "%s: b=%d n=%d", what, b, n);
+  if (d != 64 && d != 128)
+    return fail(DUSTIN_ERR_UNSUPPORTED, "%s: d=%d (64 or 128)", what, d);
+  if (n_pairs < 1 || n_pairs > kMaxPairs)
+    return fail(DUSTIN_ERR_UNSUPPORTED, "%s: n_pairs=%d (1..%d)", what, n_pairs,
+                kMaxPairs);
+  if (rows < 1 || rows > 16)
+    return fail(DUSTIN_ERR_UNSUPPORTED, "%s: rows=%d (1..16)", what, rows);
+  if (n_pairs * rows > 1024)
+    return fail(DUSTIN_ERR_UNSUPPORTED, "%s: n_pairs*rows > 1024", what);
+  if (b == 0 || n == 0) return DUSTIN_OK;
+  if (!q || !kv || !kv_head || !s_out)
+    return fail(DUSTIN_ERR_INVALID_ARG, "%s: q, kv, kv_head, s_out required", what);
+  if (!aligned16(q) || (reinterpret_cast<uintptr_t>(s_out) & 3u))
+    return fail(DUSTIN_ERR_ALIGNMENT, "%s: q needs 16-byte alignment", what);
+  if (!std::isfinite(scale))
+    return fail(DUSTIN_ERR_INVALID_ARG, "%s: scale is not finite", what);
+  if ((long long)n_pairs * b * ((n + score_chunk() - 1) / score_chunk()) > 0x7fffffffLL ||
+      (long long)b > 65535)
+    return fail(DUSTIN_ERR_SHAPE, "%s: problem too large", what);
+  bool paged = false;
+  for (int p = 0; p < n_pairs; ++p) {
+    int rc = check_kv(&kv[p], b, n, d, false, what);
+    if (rc) return rc;
+    if (kv_head[p] < 0)
+      return fail(DUSTIN_ERR_SHAPE, "%s: kv_head[%d]=%d", what, p, kv_head[p]);
+    if (p > 0 && ((kv[p].page_table != nullptr) != paged))
+      return fail(DUSTIN_ERR_UNSUPPORTED, "%s: mixed paged/contiguous pairs", what);
+    paged = kv[p].page_table != nullptr;
+  }
+  const size_t need = dustin_score_heads_workspace_size(b, n, n_pairs, rows);
+  if (!ws || ws_bytes < need || !aligned16(ws))
+    return fail(DUSTIN_ERR_WORKSPACE, "%s: workspace %zu bytes, need %zu", what,
+                ws_bytes, need);
+  ScoreArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.s_out = s_out;
+  a.b = b;
+  a.n = n;
+  a.n_pairs = n_pairs;
+  a.rows = rows;
+  a.chunk = score_chunk();
+  a.nchunks = (n + a.chunk - 1) / a.chunk;
+  a.scale_log2 = scale * kLog2e;
+  const size_t prs = (size_t)n_pairs * rows * b;
+  a.logits = static_cast<float*>(ws);
+  a.stats = reinterpret_cast<float2*>(static_cast<char*>(ws) +
+                                      align256(prs * n * sizeof(float)));
+  for (int p = 0; p < n_pairs; ++p) {
+    a.pairs[p].kv = to_view(kv[p]);
+    a.pairs[p].kv_head = kv_head[p];
+  }
+  cudaError_t e = launch_score(a, d, paged, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  return DUSTIN_OK;
+}
+
+int dustin_hybrid_topk(int b, int n, int k, int n_sink, int n_recent,
+                       double alpha, int m, int norm, const float* s_draft,
+                       const float* s_target, int32_t* idx, void* stream) {
+  const char* what = "dustin_hybrid_topk";
+  if (b < 0 || n < 0 || k < 0)
+    return fail(DUSTIN_ERR_SHAPE, "%s: b=%d n=%d k=%d", what, b, n, k);
+  if (n > kSelectMaxN)
+    return fail(DUSTIN_ERR_UNSUPPORTED, "%s: n=%d > %d", what, n, kSelectMaxN);
+  if (norm != DUSTIN_NORM_NONE && norm != DUSTIN_NORM_L1)
+    return fail(DUSTIN_ERR_INVALID_ARG, "%s: norm=%d", what, norm);
+  if (!std::isfinite(alpha))
+    return fail(DUSTIN_ERR_INVALID_ARG, "%s: alpha not finite", what);
+  if (b == 0 || n == 0 || k == 0) return DUSTIN_OK;
+  if (!idx) return fail(DUSTIN_ERR_INVALID_ARG, "%s: idx is NULL", what);
+  if (k < n) {
+    if (!s_draft && !s_target)
+      return fail(DUSTIN_ERR_INVALID_ARG, "%s: both score vectors NULL", what);
+    const int ns = std::min(std::max(n_sink, 0), n);
+    const int hi = n - std::min(std::max(n_recent, 0), n);
+    const int forced = hi <= ns ? n : ns + (n - hi);
+    if (forced > k)
+      return fail(DUSTIN_ERR_SHAPE, "%s: %d protected positions exceed k=%d", what,
+                  forced, k);
+    if (m >= 0) {
+      const int budget = k - forced;
+      const int m_eff = std::min(m, budget);
+      if (m_eff > 0 && !s_draft)
+        return fail(DUSTIN_ERR_INVALID_ARG, "%s: m mode needs s_draft", what);
+      if (budget - m_eff > 0 && !s_target)
+        return fail(DUSTIN_ERR_INVALID_ARG, "%s: m mode needs s_target", what);
+    }
+  }
+  SelectArgs a;
+  a.sd = s_draft;
+  a.st = s_target;
+  a.idx = idx;
+  a.alpha = alpha;
+  a.b = b;
+  a.n = n;
+  a.k = k;
+  a.n_sink = n_sink;
+  a.n_recent = n_recent;
+  a.m = m;
+  a.norm = norm;
+  cudaError_t e = launch_select(a, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  return DUSTIN_OK;
+}
+
+size_t dustin_sparse_verify_attn_workspace_size(int b, int h_q, int h_kv, int d,
+                                                int w, int k) {
+  if (b <= 0 || h_q <= 0 || h_kv <= 0 || h_q % h_kv || w <= 0 || k < 0 ||
+      (d != 64 && d != 128))
+    return 0;
+  AttnPlan p = plan_attn(false, b, h_q, h_kv, d, w, k);
+  return p.ws_o + p.ws_ml;
+}
+
+int dustin_sparse_verify_attn(int b, int h_q, int h_kv, int d, int w, int n,
+                              int k, const void* q, const dustin_kv* kv,
+                              const int32_t* idx, float scale, void* o,
+                              float* lse, void* ws, size_t ws_bytes,
+                              void* stream) {
+  return run_attn(false, b, h_q, h_kv, d, w, n, k, q, kv, idx, scale, o, lse, ws,
+                  ws_bytes, stream);
+}
+
+size_t dustin_full_verify_attn_workspace_size(int b, int h_q, int h_kv, int d,
+                                              int w, int n) {
+  if (b <= 0 || h_q <= 0 || h_kv <= 0 || h_q % h_kv || w <= 0 || n < 0 ||
+      (d != 64 && d != 128))
+    return 0;
+  AttnPlan p = plan_attn(true, b, h_q, h_kv, d, w, n);
+  return p.ws_o + p.ws_ml;
+}
+
+int dustin_full_verify_attn(int b, int h_q, int h_kv, int d, int w, int n,
+                            const void* q, const dustin_kv* kv, float scale,
+                            void* o, float* lse, void* ws, size_t ws_bytes,
+                            void* stream) {
+  return run_attn(true, b, h_q, h_kv, d, w, n, n, q, kv, nullptr, scale, o, lse,
+                  ws, ws_bytes, stream);
+}
+
+}  // extern "C"

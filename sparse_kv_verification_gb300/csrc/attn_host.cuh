@@ -1,0 +1,110 @@
+// Host-side launch of the verification-attention kernels (one instance set
+// per translation unit: sparse or dense).
+#pragma once
+
+#include <atomic>
+
+#include "attn.cuh"
+#include "internal.h"
+
+namespace dustin {
+
+// Sets the dynamic shared-memory limit of `kern` once per device.
+template <typename K>
+cudaError_t ensure_smem_attr(K kern, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           bytes);
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
+template <bool DENSE>
+struct AttnHost {
+  template <int D, int MT, bool PAGED>
+  static cudaError_t prepare() {
+    static std::atomic<uint64_t> done{0};
+    return ensure_smem_attr(verify_attn_kernel<D, MT, PAGED, DENSE>,
+                            AttnCfg<D, MT>::SMEM, done);
+  }
+
+  template <int D, int MT, bool PAGED>
+  static cudaError_t run(const AttnArgs& a, cudaStream_t st) {
+    using C = AttnCfg<D, MT>;
+    cudaError_t e = prepare<D, MT, PAGED>();
+    if (e != cudaSuccess) return e;
+    const long long blocks = (long long)a.b * a.hkv * a.row_blocks;
+    verify_attn_kernel<D, MT, PAGED, DENSE>
+        <<<(unsigned)(blocks * a.splits), C::NT, C::SMEM, st>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    note_launches(1);
+    if (a.splits > 1) {
+      const long long warps = blocks * C::ROWS;
+      attn_combine_kernel<D, MT><<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(a);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+      note_launches(1);
+    }
+    return cudaSuccess;
+  }
+
+  template <int D, bool PAGED>
+  static cudaError_t by_mt(const AttnArgs& a, int mt, cudaStream_t st) {
+    switch (mt) {
+      case 1: return run<D, 1, PAGED>(a, st);
+      case 2: return run<D, 2, PAGED>(a, st);
+      case 3: return run<D, 3, PAGED>(a, st);
+      default: return run<D, 4, PAGED>(a, st);
+    }
+  }
+
+  static cudaError_t launch(const AttnArgs& a, int d, int mt, bool paged,
+                            cudaStream_t st) {
+    if (d == 64) return paged ? by_mt<64, true>(a, mt, st) : by_mt<64, false>(a, mt, st);
+    return paged ? by_mt<128, true>(a, mt, st) : by_mt<128, false>(a, mt, st);
+  }
+
+  template <int D, int MT>
+  static int occ() {
+    if (prepare<D, MT, false>() != cudaSuccess) return 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &n, verify_attn_kernel<D, MT, false, DENSE>, AttnCfg<D, MT>::NT,
+            AttnCfg<D, MT>::SMEM) != cudaSuccess)
+      return 1;
+    return n > 0 ? n : 1;
+  }
+
+  static int occupancy(int d, int mt) {
+    if (d == 64) {
+      switch (mt) {
+        case 1: return occ<64, 1>();
+        case 2: return occ<64, 2>();
+        case 3: return occ<64, 3>();
+        default: return occ<64, 4>();
+      }
+    }
+    switch (mt) {
+      case 1: return occ<128, 1>();
+      case 2: return occ<128, 2>();
+      case 3: return occ<128, 3>();
+      default: return occ<128, 4>();
+    }
+  }
+
+  static cudaError_t take_flags(unsigned* flags) {
+    unsigned v = 0, zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_attn_dev_flags, sizeof(v));
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpyToSymbol(g_attn_dev_flags, &zero, sizeof(zero));
+    *flags |= v;
+    return e;
+  }
+};
+
+}  // namespace dustin

@@ -1,0 +1,61 @@
+// Host-side declarations shared by the C-ABI layer (api.cu) and the kernel
+// translation units.  Not part of the public interface.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "device_common.cuh"
+
+namespace dustin {
+
+// ---- scoring
+constexpr int kMaxPairs = 64;
+
+struct ScorePair {
+  KvView kv;
+  int kv_head;
+};
+
+struct ScoreArgs {
+  const __nv_bfloat16* q;  // [n_pairs][b][rows][d]
+  float* s_out;            // [b][n]
+  float* logits;           // workspace [n_pairs][rows][b][n], log2 units
+  float2* stats;           // workspace [n_pairs][rows][b][nchunks]
+  int b, n, n_pairs, rows;
+  int chunk, nchunks;
+  float scale_log2;
+  ScorePair pairs[kMaxPairs];
+};
+
+int score_chunk();
+cudaError_t launch_score(const ScoreArgs& a, int d, bool paged, cudaStream_t st);
+cudaError_t take_score_flags(unsigned* flags);
+
+// ---- selection
+struct SelectArgs {
+  const float* sd;
+  const float* st;
+  int32_t* idx;
+  double alpha;
+  int b, n, k, n_sink, n_recent, m, norm;
+};
+constexpr int kSelectMaxN = 1 << 20;
+cudaError_t launch_select(const SelectArgs& a, cudaStream_t st);
+
+// ---- verification attention (declared in attn.cuh: AttnArgs)
+struct AttnArgs;
+cudaError_t launch_attn_sparse(const AttnArgs& a, int d, int mt, bool paged,
+                               cudaStream_t st);
+cudaError_t launch_attn_dense(const AttnArgs& a, int d, int mt, bool paged,
+                              cudaStream_t st);
+int occupancy_attn_sparse(int d, int mt);
+int occupancy_attn_dense(int d, int mt);
+cudaError_t take_attn_sparse_flags(unsigned* flags);
+cudaError_t take_attn_dense_flags(unsigned* flags);
+
+// ---- bookkeeping (api.cu)
+void note_launches(int count);
+
+}  // namespace dustin

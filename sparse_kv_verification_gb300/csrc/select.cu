@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectArgs a) {
     const bool keep = j < n && (forced(j) || ((bits[j >> 5] >> (j & 31)) & 1u));
     int tot;
     const int pos = block_scan(keep ? 1 : 0, sh.warp_sums, &tot);
-    if (keep) out[written + pos] = j;
+    if (keep && written + pos < k) out[written + pos] = j;
     written += tot;
   }
 }

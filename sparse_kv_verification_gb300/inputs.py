@@ -322,3 +322,71 @@ def to_paged(keys: torch.Tensor, values: Optional[torch.Tensor],
 
     return scatter(keys), (scatter(values) if values is not None else None), \
         table.to(keys.device)
+
+
+# ------------------------------------------------------------ one decode step
+
+@dataclasses.dataclass
+class StepInputs:
+    """Every tensor one pass of the hot path reads, for one workload.
+
+    q[i], k[i], v[i]: target layer ``layer_ids[i]``'s verification queries
+    [b][hq][w][d] and KV [b][hkv][n][d].  q_t [p_t][b][1][d] are the scored
+    target heads' latest-token queries, k_t[p] the key cache their pair reads
+    at kv head kvh_t[p].  q_d [p_d][b][gamma][dd] and k_d / kvh_d likewise for
+    the draft's lookahead queries."""
+    wl: Workload
+    layer_ids: List[int]
+    q: List[torch.Tensor]
+    k: List[torch.Tensor]
+    v: List[torch.Tensor]
+    pairs_t: List[Tuple[int, int]]
+    pairs_d: List[Tuple[int, int]]
+    q_t: torch.Tensor
+    k_t: List[torch.Tensor]
+    kvh_t: List[int]
+    q_d: torch.Tensor
+    k_d: List[torch.Tensor]
+    kvh_d: List[int]
+    hh: torch.Tensor
+
+
+def step_inputs(wl: Workload, device="cpu", n_layers: Optional[int] = None
+                ) -> StepInputs:
+    """Materialises ``n_layers`` target layers (default: all) and the draft
+    layers the scored pairs use.  With fewer layers than the model has, a
+    scored pair at layer l reads layer l % n_layers."""
+    n_layers = wl.layers if n_layers is None else max(1, min(n_layers,
+                                                             wl.layers))
+    hh = heavy_hitter_positions(wl, device)
+    layer_ids = list(range(n_layers))
+    qs, ks, vs = [], [], []
+    for l in layer_ids:
+        q, k, v = target_layer(wl, l, device, hh)
+        qs.append(q)
+        ks.append(k)
+        vs.append(v)
+    pairs_t, pairs_d = scored_pairs(wl)
+    pairs_t = [(l % n_layers, h) for l, h in pairs_t]
+    q_t_list, kvh_t = [], []
+    hh_hist = drifted_positions(wl, hh)
+    for l, h in pairs_t:
+        qh = historical_query(wl, qs[l], h, device)
+        ks[l] = plant_historical(wl, ks[l], qh, h // wl.group, hh_hist)
+        q_t_list.append(qh)
+        kvh_t.append(h // wl.group)
+    k_t = [ks[l] for l, _ in pairs_t]
+    draft = {}
+    for l, _ in pairs_d:
+        if l not in draft:
+            draft[l] = draft_layer(wl, l, device, hh)
+    q_d = torch.stack([draft[l][0][:, h] for l, h in pairs_d]) if pairs_d \
+        else torch.zeros((0, wl.b, max(wl.gamma, 1), wl.draft_d),
+                         dtype=torch.bfloat16, device=device)
+    k_d = [draft[l][1] for l, _ in pairs_d]
+    kvh_d = [h // wl.draft_group for _, h in pairs_d]
+    q_t = torch.stack(q_t_list) if q_t_list else torch.zeros(
+        (0, wl.b, 1, wl.d), dtype=torch.bfloat16, device=device)
+    return StepInputs(wl, layer_ids, qs, ks, vs, pairs_t, pairs_d,
+                      q_t.contiguous(), k_t, kvh_t, q_d.contiguous(), k_d,
+                      kvh_d, hh)

@@ -1,0 +1,252 @@
+"""GPU parity: the CUDA path (through the C-ABI) against the CPU oracle on
+the same seeded inputs, at sizes the oracle finishes in seconds that span
+several tiles, ragged tails, every kernel variant and the edge cases."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import dustin_oracle as O
+from sparse_kv_verification_gb300 import build, inputs as I, native as N
+from tests import gpu_harness as H
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    build.build()
+    return N.load()
+
+
+def qkv(b, hq, hkv, d, w, n, seed):
+    g = I.generator(seed)
+    q = torch.randn((b, hq, w, d), generator=g).to(torch.bfloat16)
+    k = torch.randn((b, hkv, n, d), generator=g).to(torch.bfloat16)
+    v = torch.randn((b, hkv, n, d), generator=g).to(torch.bfloat16)
+    return q, k, v
+
+
+# (b, h_q, h_kv, d, w, n, k): 16-row tiles 1..4, two row blocks, d 64/128,
+# ragged n and k, one sequence with many splits, k past the 2048 split cap.
+SHAPES = [
+    (1, 4, 2, 64, 4, 256, 32),
+    (2, 28, 4, 128, 4, 700, 131),
+    (3, 40, 8, 128, 5, 1000, 333),
+    (2, 64, 8, 128, 5, 3000, 1100),
+    (1, 64, 8, 128, 8, 2048, 600),
+    (1, 64, 4, 64, 5, 900, 450),
+    (1, 8, 1, 128, 3, 5000, 4500),
+    (4, 14, 2, 64, 4, 129, 65),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=[str(s) for s in SHAPES])
+def test_sparse_attention_parity(shape):
+    b, hq, hkv, d, w, n, k = shape
+    q, kk, v = qkv(b, hq, hkv, d, w, n, seed=sum(shape))
+    idx = I.random_sorted_indices(b, n, k, seed=k + n)
+    scale = d ** -0.5
+    o, lse = H.sparse_attn(q.to(DEV), kk.to(DEV), v.to(DEV), idx.to(DEV), scale)
+    o_ref, lse_ref = O.verify_attention(H.f64(q), H.f64(kk), H.f64(v),
+                                        idx.numpy(), scale)
+    H.assert_attn_close(o, lse, o_ref, lse_ref)
+
+
+@pytest.mark.parametrize("shape", SHAPES[:6], ids=[str(s) for s in SHAPES[:6]])
+def test_full_attention_parity(shape):
+    b, hq, hkv, d, w, n, _ = shape
+    q, kk, v = qkv(b, hq, hkv, d, w, n, seed=sum(shape) + 1)
+    scale = d ** -0.5
+    o, lse = H.full_attn(q.to(DEV), kk.to(DEV), v.to(DEV), scale)
+    o_ref, lse_ref = O.full_verify_attention(H.f64(q), H.f64(kk), H.f64(v),
+                                             scale)
+    H.assert_attn_close(o, lse, o_ref, lse_ref)
+
+
+def test_sparse_with_all_positions_matches_full():
+    b, hq, hkv, d, w, n = 2, 16, 2, 128, 4, 777
+    q, kk, v = qkv(b, hq, hkv, d, w, n, seed=5)
+    q, kk, v = q.to(DEV), kk.to(DEV), v.to(DEV)
+    idx = torch.arange(n, dtype=torch.int32, device=DEV).repeat(b, 1)
+    o1, l1 = H.sparse_attn(q, kk, v, idx.contiguous(), 0.1)
+    o2, l2 = H.full_attn(q, kk, v, 0.1)
+    assert (o1.float() - o2.float()).abs().max().item() <= 1e-2
+    assert (l1 - l2).abs().max().item() <= 1e-4
+
+
+@pytest.mark.parametrize("page", [16, 32])
+def test_paged_layout_matches_contiguous_and_oracle(page):
+    b, hq, hkv, d, w, n, k = 2, 16, 2, 128, 4, 1000, 300
+    q, kk, v = qkv(b, hq, hkv, d, w, n, seed=page)
+    pk, pv, table = I.to_paged(kk, v, page, seed=page + 1)
+    idx = I.random_sorted_indices(b, n, k, seed=3).to(DEV)
+    qd = q.to(DEV)
+    o_c, l_c = H.sparse_attn(qd, kk.to(DEV), v.to(DEV), idx, 0.1)
+    o_p, l_p = H.sparse_attn(qd, pk.to(DEV), pv.to(DEV), idx, 0.1, n=n,
+                             page_table=table.to(DEV))
+    assert torch.equal(o_c, o_p) and torch.equal(l_c, l_p)
+    o_ref, l_ref = O.verify_attention(H.f64(q), H.f64(kk), H.f64(v),
+                                      idx.cpu().numpy(), 0.1)
+    H.assert_attn_close(o_p, l_p, o_ref, l_ref)
+    f_c, fl_c = H.full_attn(qd, kk.to(DEV), v.to(DEV), 0.1)
+    f_p, fl_p = H.full_attn(qd, pk.to(DEV), pv.to(DEV), 0.1, n=n,
+                            page_table=table.to(DEV))
+    assert torch.equal(f_c, f_p) and torch.equal(fl_c, fl_p)
+
+
+def test_attention_edge_cases():
+    q, kk, v = qkv(2, 8, 2, 64, 3, 50, seed=9)
+    q, kk, v = q.to(DEV), kk.to(DEV), v.to(DEV)
+    # k = 0: empty selection gives O = 0, LSE = -inf.
+    o, lse = H.sparse_attn(q, kk, v, torch.zeros((2, 0), dtype=torch.int32,
+                                                 device=DEV), 0.2)
+    assert torch.all(o == 0) and torch.all(lse == float("-inf"))
+    # n smaller than one tile, k = n.
+    idx = torch.arange(50, dtype=torch.int32, device=DEV).repeat(2, 1)
+    o, lse = H.sparse_attn(q, kk, v, idx.contiguous(), 0.2)
+    o_ref, l_ref = O.full_verify_attention(H.f64(q), H.f64(kk), H.f64(v), 0.2)
+    H.assert_attn_close(o, lse, o_ref, l_ref)
+    # One position only.
+    one = torch.tensor([[7], [49]], dtype=torch.int32, device=DEV)
+    o, lse = H.sparse_attn(q, kk, v, one, 0.2)
+    o_ref, l_ref = O.verify_attention(H.f64(q), H.f64(kk), H.f64(v),
+                                      one.cpu().numpy(), 0.2)
+    H.assert_attn_close(o, lse, o_ref, l_ref)
+
+
+def test_out_of_range_index_is_flagged_not_faulted():
+    """The kernel's own bounds check: an index >= n is left out of the
+    attention and raises a device flag; no access goes out of bounds."""
+    q, kk, v = qkv(1, 4, 1, 64, 2, 100, seed=11)
+    N.dustin_device_status()                     # clear old flags
+    idx = torch.tensor([[3, 10, 200, 50]], dtype=torch.int32)
+    o, lse = H.sparse_attn(q.to(DEV), kk.to(DEV), v.to(DEV), idx.to(DEV), 0.2)
+    flags = N.dustin_device_status()
+    assert flags & 1
+    o_ref, l_ref = O.verify_attention(H.f64(q), H.f64(kk), H.f64(v),
+                                      np.array([[3, 10, 50]]), 0.2)
+    H.assert_attn_close(o, lse, o_ref, l_ref)
+    assert N.dustin_device_status() == 0          # read clears
+
+
+# ---------------------------------------------------------------- scoring
+
+@pytest.mark.parametrize("p,b,rows,d,n", [(4, 2, 1, 128, 3000),
+                                          (3, 2, 4, 64, 1000),
+                                          (2, 1, 16, 128, 200),
+                                          (1, 3, 3, 64, 4097)])
+def test_score_heads_parity(p, b, rows, d, n):
+    g = I.generator(p * 100 + n)
+    q = torch.randn((p, b, rows, d), generator=g).to(torch.bfloat16)
+    hkv = 3
+    keys = [(2.0 * torch.randn((b, hkv, n, d), generator=g)).to(torch.bfloat16)
+            for _ in range(p)]
+    heads = [i % hkv for i in range(p)]
+    scale = d ** -0.5
+    s = H.score(q.to(DEV), [k.to(DEV) for k in keys], heads, scale, n)
+    ref = O.score_heads([H.f64(q[i]) for i in range(p)],
+                        [H.f64(keys[i][:, heads[i]]) for i in range(p)], scale)
+    np.testing.assert_allclose(H.f64(s), ref, rtol=2e-4, atol=1e-7)
+    np.testing.assert_allclose(H.f64(s).sum(axis=1), p * rows, rtol=1e-4)
+
+
+def test_score_heads_paged_matches_contiguous():
+    p, b, rows, d, n = 2, 2, 2, 128, 1500
+    g = I.generator(77)
+    q = torch.randn((p, b, rows, d), generator=g).to(torch.bfloat16).to(DEV)
+    keys = [torch.randn((b, 2, n, d), generator=g).to(torch.bfloat16)
+            for _ in range(p)]
+    paged = [I.to_paged(k, None, 16, seed=i) for i, k in enumerate(keys)]
+    s_c = H.score(q, [k.to(DEV) for k in keys], [0, 1], 0.1, n)
+    s_p = H.score(q, [pk.to(DEV) for pk, _, _ in paged], [0, 1], 0.1, n,
+                  page_tables=[t.to(DEV) for _, _, t in paged])
+    assert torch.equal(s_c, s_p)
+
+
+# ---------------------------------------------------------------- selection
+
+SELECT_CASES = [
+    # b, n, k, n_sink, n_recent, alpha, m, norm, specials
+    (3, 1000, 100, 4, 64, 0.5, -1, 1, False),
+    (2, 32768, 2048, 4, 64, 0.5, -1, 1, True),
+    (4, 5000, 700, 0, 0, 1.0, -1, 0, True),
+    (2, 4096, 300, 2, 8, 0.0, -1, 1, False),
+    (2, 3000, 500, 4, 16, 0.25, -1, 0, True),
+    (2, 3000, 500, 4, 16, 0.5, 100, 1, False),
+    (2, 3000, 500, 4, 16, 0.5, 0, 1, True),
+    (2, 3000, 500, 4, 16, 0.5, 1000, 1, False),
+    (1, 100, 100, 2, 2, 0.5, -1, 1, False),
+    (1, 100, 250, 2, 2, 0.5, -1, 1, False),
+    (2, 100, 12, 4, 8, 0.5, -1, 1, False),
+    (1, 1, 1, 0, 0, 0.5, -1, 1, False),
+    (3, 17, 5, 0, 0, 0.5, -1, 1, False),
+    (2, 65536, 8192, 4, 64, 0.5, -1, 1, True),
+]
+
+
+@pytest.mark.parametrize("case", SELECT_CASES, ids=[str(c) for c in SELECT_CASES])
+def test_select_bit_exact(case):
+    b, n, k, ns, nr, alpha, m, norm, specials = case
+    sd = I.synthetic_scores(b, n, seed=n + k, specials=specials)
+    st = I.synthetic_scores(b, n, seed=n + k + 1, specials=specials)
+    got = H.select(sd.to(DEV), st.to(DEV), k, ns, nr, alpha, m, norm)
+    want = O.hybrid_select(sd.numpy(), st.numpy(), k, ns, nr, alpha, m, norm)
+    np.testing.assert_array_equal(got.cpu().numpy(), want)
+
+
+def test_select_single_vector():
+    sd = I.synthetic_scores(2, 2000, seed=1)
+    got = H.select(sd.to(DEV), None, 100, 4, 4, 1.0, -1, 0)
+    want = O.hybrid_select(sd.numpy(), None, 100, 4, 4, 1.0, -1, 0)
+    np.testing.assert_array_equal(got.cpu().numpy(), want)
+    # alpha = 1, NONE, no target: the vector passes through unchanged, so
+    # the result is the Top-K of the raw vector.
+    forced = O.protected_positions(2000, 4, 4)
+    elig = np.ones(2000, bool)
+    elig[forced] = False
+    for r in range(2):
+        raw = np.sort(np.concatenate([forced, O.topk(sd[r].numpy(), 92, elig)]))
+        np.testing.assert_array_equal(got[r].cpu().numpy(), raw)
+    st = I.synthetic_scores(2, 2000, seed=2)
+    got = H.select(None, st.to(DEV), 100, 4, 4, 0.0, -1, 1)
+    want = O.hybrid_select(None, st.numpy(), 100, 4, 4, 0.0, -1, 1)
+    np.testing.assert_array_equal(got.cpu().numpy(), want)
+
+
+# ---------------------------------------------------------------- the chain
+
+def test_tiny_chain_score_select_attend():
+    """The tiny workload end to end: scores match, the index set equals the
+    oracle's, attention matches, windowed ARR agrees."""
+    wl = I.WORKLOADS["tiny"]
+    st_in = I.step_inputs(wl, "cpu")
+    s_t = H.score(st_in.q_t.to(DEV), [k.to(DEV) for k in st_in.k_t],
+                  st_in.kvh_t, wl.scale, wl.n)
+    s_d = H.score(st_in.q_d.to(DEV), [k.to(DEV) for k in st_in.k_d],
+                  st_in.kvh_d, wl.draft_scale, wl.n)
+    ref_t = O.score_heads([H.f64(st_in.q_t[i]) for i in range(wl.p_t)],
+                          [H.f64(k[:, h]) for k, h in zip(st_in.k_t,
+                                                          st_in.kvh_t)],
+                          wl.scale)
+    ref_d = O.score_heads([H.f64(st_in.q_d[i]) for i in range(wl.p_d)],
+                          [H.f64(k[:, h]) for k, h in zip(st_in.k_d,
+                                                          st_in.kvh_d)],
+                          wl.draft_scale)
+    np.testing.assert_allclose(H.f64(s_t), ref_t, rtol=2e-4, atol=1e-7)
+    np.testing.assert_allclose(H.f64(s_d), ref_d, rtol=2e-4, atol=1e-7)
+    idx = H.select(s_d, s_t, wl.k, wl.n_sink, wl.n_recent, wl.alpha, -1, 1)
+    idx_ref = O.hybrid_select(ref_d, ref_t, wl.k, wl.n_sink, wl.n_recent,
+                              wl.alpha, -1, 1)
+    np.testing.assert_array_equal(idx.cpu().numpy(), idx_ref)
+    q, k, v = st_in.q[0], st_in.k[0], st_in.v[0]
+    o, lse = H.sparse_attn(q.to(DEV), k.to(DEV), v.to(DEV), idx, wl.scale)
+    o_ref, l_ref = O.verify_attention(H.f64(q), H.f64(k), H.f64(v), idx_ref,
+                                      wl.scale)
+    H.assert_attn_close(o, lse, o_ref, l_ref)
+    a = np.stack([O.attention_weights(H.f64(q)[0, h], H.f64(k)[0, h // 2],
+                                      wl.scale) for h in range(wl.hq)])
+    got = np.mean([O.windowed_arr(a[h], idx.cpu().numpy()[0])
+                   for h in range(wl.hq)])
+    want = np.mean([O.windowed_arr(a[h], idx_ref[0]) for h in range(wl.hq)])
+    assert abs(got - want) <= H.ARR_TOL

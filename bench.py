@@ -1,0 +1,544 @@
+#!/usr/bin/env python3
+"""Benchmark of the Dustin sparse-verification hot path on GB300.
+
+One step is one pass of the whole hot path over one batch: score the
+target's scored heads (S_Target), score the draft's (S_Draft), the hybrid
+Top-K, then the sparse verification attention of every target layer over the
+selected KV.  The metric is verified tokens per second per layer,
+b * w * layers / step time, on the Qwen2.5-72B-shaped workload (b16, n32768,
+w5, k2048, 80 layers, 4 + 4 scored pairs).  The KV cache (172 GB) is resident
+in HBM: each step's queries are the per-step inputs.  Inputs are larger than
+L2 (80 distinct 2.1 GB layers per step), so no flush is needed.
+
+Also reported: the dense full-cache verification (the in-run baseline),
+per-kernel times, the roofline of the sparse attention kernel, an end-to-end
+number with the queries copied from pinned host memory and the outputs read
+back every step, SM clocks during the timed region, and the CPU oracle timed
+on a bounded sample of the same workload.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+Under torchrun each rank runs an independent replica (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = ("verified tokens/s per layer, 72B-shape 32k×b16 k=2048; "
+          "HBM GB/s vs peak")
+UNIT = "tokens/s/layer"
+FALLBACK_HBM_GBS = 6800.0
+ATTN_SOURCES = ("attn.cuh", "attn_host.cuh", "device_common.cuh",
+                "attn_sparse.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "sparse_verify_attn_72b.md")
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--config", default="72b")
+    p.add_argument("--layers", type=int, default=None,
+                   help="target layers to materialise (default: all)")
+    p.add_argument("--batch", type=int, default=None,
+                   help="override the batch (sequences per GPU)")
+    p.add_argument("--dense-steps", type=int, default=3)
+    p.add_argument("--no-dense", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--cpu-rows", type=int, default=1)
+    p.add_argument("--cpu-layers", type=int, default=2)
+    p.add_argument("--cpu-reps", type=int, default=2)
+    p.add_argument("--oracle-worker", action="store_true",
+                   help=argparse.SUPPRESS)
+    return p.parse_args(argv)
+
+
+# ----------------------------------------------------------------- helpers
+
+def measured_peak_gbs():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def attn_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ATTN_SOURCES:
+        with open(os.path.join(ROOT, "sparse_kv_verification_gb300", "csrc",
+                               name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic():
+    """DRAM bytes per launch of the sparse attention kernel from the
+    committed ncu summary, if it was taken on the current kernel source."""
+    try:
+        text = open(TRAFFIC_FILE).read()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("source_sha") != attn_source_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch_full"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,"
+             "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv",
+                                                    delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index),
+                 f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "note": "nvidia-smi unavailable"}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except (ValueError, IndexError):
+                continue
+            for i, name in enumerate(names):
+                if len(r) > 5 + i and r[5 + i].strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- replica
+
+class Replica:
+    """One GPU's copy of the workload with pre-marshalled library calls."""
+
+    def __init__(self, wl, device, n_layers):
+        import torch
+        from sparse_kv_verification_gb300 import inputs as I
+        from sparse_kv_verification_gb300 import native as N
+        self.wl, self.dev = wl, device
+        inp = I.step_inputs(wl, device, n_layers)
+        self.inp = inp
+        self.L = len(inp.layer_ids)
+        b, n = wl.b, wl.n
+        self.s_t = torch.empty((b, n), device=device)
+        self.s_d = torch.empty((b, n), device=device)
+        self.idx = torch.empty((b, min(wl.k, n)), dtype=torch.int32,
+                               device=device)
+        self.o = [torch.empty_like(q) for q in inp.q]
+        self.lse = [torch.empty(q.shape[:3], device=device) for q in inp.q]
+        self.ws_t = N.workspace(N.dustin_score_heads_workspace_size(
+            b, n, wl.p_t, 1), device)
+        self.ws_d = N.workspace(N.dustin_score_heads_workspace_size(
+            b, n, wl.p_d, wl.gamma), device)
+        self.ws_a = N.workspace(N.dustin_sparse_verify_attn_workspace_size(
+            b, wl.hq, wl.hkv, wl.d, wl.w, wl.k), device)
+        self.ws_f = N.workspace(N.dustin_full_verify_attn_workspace_size(
+            b, wl.hq, wl.hkv, wl.d, wl.w, n), device)
+        kv = [N.kv_desc(k, v) for k, v in zip(inp.k, inp.v)]
+        self.score_t = N.prepare_score_heads(
+            inp.q_t, [N.kv_desc(k) for k in inp.k_t], inp.kvh_t, wl.scale,
+            self.s_t, self.ws_t, n)
+        self.score_d = N.prepare_score_heads(
+            inp.q_d, [N.kv_desc(k) for k in inp.k_d], inp.kvh_d,
+            wl.draft_scale, self.s_d, self.ws_d, n)
+        self.select = N.prepare_hybrid_topk(
+            self.s_d, self.s_t, wl.k, wl.n_sink, wl.n_recent, wl.alpha, wl.m,
+            N.DUSTIN_NORM_L1, self.idx)
+        self.attn = [N.prepare_sparse_verify_attn(
+            inp.q[l], kv[l], wl.hkv, n, self.idx, wl.scale, self.o[l],
+            self.lse[l], self.ws_a) for l in range(self.L)]
+        self.full = [N.prepare_full_verify_attn(
+            inp.q[l], kv[l], wl.hkv, n, wl.scale, self.o[l], self.lse[l],
+            self.ws_f) for l in range(self.L)]
+
+    def step(self, ev=None):
+        """One pass of the hot path; ev (optional) records per-phase events:
+        ev[0..3] around score/select, ev[4 + 2l], ev[5 + 2l] around layer l."""
+        if ev is None:
+            self.score_t()
+            self.score_d()
+            self.select()
+            for a in self.attn:
+                a()
+            return
+        ev[0].record()
+        self.score_t()
+        ev[1].record()
+        self.score_d()
+        ev[2].record()
+        self.select()
+        ev[3].record()
+        for l, a in enumerate(self.attn):
+            ev[4 + 2 * l].record()
+            a()
+            ev[5 + 2 * l].record()
+
+    # Algorithmic bytes (what the method must move), per launch / per step.
+    def bytes_sparse_launch(self):
+        wl = self.wl
+        kk = min(wl.k, wl.n)
+        return (wl.b * wl.hkv * kk * wl.d * 2 * 2 +          # K, V rows
+                2 * wl.b * wl.hq * wl.w * wl.d * 2 +           # Q in, O out
+                wl.b * wl.hq * wl.w * 4 + wl.b * kk * 4)       # LSE, idx
+
+    def bytes_dense_launch(self):
+        wl = self.wl
+        return (wl.b * wl.hkv * wl.n * wl.d * 2 * 2 +
+                2 * wl.b * wl.hq * wl.w * wl.d * 2 + wl.b * wl.hq * wl.w * 4)
+
+    def bytes_score_t(self):
+        wl = self.wl
+        return (wl.p_t * wl.b * wl.n * wl.d * 2 + wl.p_t * wl.b * wl.d * 2 +
+                wl.b * wl.n * 4)
+
+    def bytes_score_d(self):
+        wl = self.wl
+        return (wl.p_d * wl.b * wl.n * wl.draft_d * 2 +
+                wl.p_d * wl.b * wl.gamma * wl.draft_d * 2 + wl.b * wl.n * 4)
+
+    def bytes_select(self):
+        wl = self.wl
+        return 2 * wl.b * wl.n * 4 + wl.b * min(wl.k, wl.n) * 4
+
+
+# ----------------------------------------------------------------- oracle leg
+
+def oracle_worker(args):
+    """Runs inside a fresh single-threaded process: the CPU oracle on a
+    bounded sample (a few sequences, a few layers) of the workload."""
+    import numpy as np
+    import torch
+    torch.set_num_threads(1)
+    from oracle import dustin_oracle as O
+    from sparse_kv_verification_gb300 import inputs as I
+    wl = I.WORKLOADS[args.config]
+    if args.batch:
+        wl = wl.replace(b=args.batch)
+    full_layers = wl.layers
+    sample = wl.replace(b=args.cpu_rows)
+    inp = I.step_inputs(sample, "cpu", args.cpu_layers)
+    f = lambda t: t.to(torch.float64).numpy()
+    q_t = [f(inp.q_t[i]) for i in range(sample.p_t)]
+    k_t = [f(k[:, h]) for k, h in zip(inp.k_t, inp.kvh_t)]
+    q_d = [f(inp.q_d[i]) for i in range(sample.p_d)]
+    k_d = [f(k[:, h]) for k, h in zip(inp.k_d, inp.kvh_d)]
+    layers = [(f(q), f(k), f(v)) for q, k, v in zip(inp.q, inp.k, inp.v)]
+    times = []
+    for _ in range(args.warmup + args.cpu_reps):
+        t0 = time.perf_counter()
+        s_t = O.score_heads(q_t, k_t, sample.scale)
+        s_d = O.score_heads(q_d, k_d, sample.draft_scale)
+        t1 = time.perf_counter()
+        idx = O.hybrid_select(s_d, s_t, sample.k, sample.n_sink,
+                              sample.n_recent, sample.alpha, sample.m,
+                              O.NORM_L1)
+        t2 = time.perf_counter()
+        for q, k, v in layers:
+            O.verify_attention(q, k, v, idx, sample.scale)
+        t3 = time.perf_counter()
+        times.append((t1 - t0, t2 - t1, (t3 - t2) / len(layers)))
+    times = times[args.warmup:]
+    t_score = statistics.median(t[0] for t in times)
+    t_sel = statistics.median(t[1] for t in times)
+    t_attn = statistics.median(t[2] for t in times)
+    t_step = t_score + t_sel + full_layers * t_attn
+    value = sample.b * sample.w * full_layers / t_step
+    print(json.dumps({
+        "value": value, "t_step_s": t_step, "t_score_s": t_score,
+        "t_select_s": t_sel, "t_attn_layer_s": t_attn,
+        "wall_s": sum(sum(t[:2]) + t[2] * len(layers) for t in times),
+        "sample": (f"{sample.b} of {wl.b} sequences, {len(layers)} of "
+                   f"{full_layers} layers timed ({args.cpu_reps} reps, median),"
+                   f" attention extrapolated to {full_layers} layers; "
+                   "single-threaded numpy fp64")}))
+
+
+def run_oracle_leg(args, reps, warmup):
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1",
+               MKL_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-worker",
+           "--config", args.config, "--cpu-rows", str(args.cpu_rows),
+           "--cpu-layers", str(args.cpu_layers), "--cpu-reps", str(reps),
+           "--warmup", str(warmup)]
+    if args.batch:
+        cmd += ["--batch", str(args.batch)]
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env)
+    if r.returncode != 0:
+        raise RuntimeError("oracle leg failed:\n" + r.stderr[-2000:])
+    out = json.loads(r.stdout.strip().splitlines()[-1])
+    out["cores"] = 1
+    return out
+
+
+# ----------------------------------------------------------------- arms
+
+def workload_config(wl, n_layers):
+    return {"workload": (f"{wl.name}: Qwen2.5-shaped target h_q{wl.hq}/h_kv"
+                         f"{wl.hkv} d{wl.d}, 0.5B-shaped draft h_q{wl.draft_hq}"
+                         f"/h_kv{wl.draft_hkv} d{wl.draft_d}; b{wl.b} n{wl.n} "
+                         f"w{wl.w} k{wl.k}; {n_layers} layers; {wl.p_t}+"
+                         f"{wl.p_d} scored pairs; alpha {wl.alpha}; "
+                         f"{wl.n_sink} sinks + {wl.n_recent} recent"),
+            "b": wl.b, "n": wl.n, "w": wl.w, "k": wl.k, "layers": n_layers,
+            "h_q": wl.hq, "h_kv": wl.hkv, "d": wl.d,
+            "l2": "inputs larger than L2: every step reads 80 distinct layers "
+                  "of 2.1 GB KV",
+            "parallelism": "replicas: each GPU runs its own batch, no "
+                           "data-path collective"}
+
+
+def run_reference(args):
+    from sparse_kv_verification_gb300 import inputs as I
+    from sparse_kv_verification_gb300 import replicas as R
+    rank, _, world = R.env_rank()
+    if rank != 0:
+        return 0
+    wl = I.WORKLOADS[args.config]
+    if args.batch:
+        wl = wl.replace(b=args.batch)
+    res = run_oracle_leg(args, max(1, args.steps), max(0, args.warmup))
+    line = {"impl": "reference", "metric": METRIC, "value": res["value"],
+            "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": res["t_step_s"] * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": workload_config(wl, wl.layers),
+            "cpu_baseline": {"value": res["value"], "unit": UNIT,
+                             "cores": res["cores"], "kind": "oracle",
+                             "sample": res["sample"]},
+            "e2e": {"value": res["value"], "unit": UNIT,
+                    "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    from sparse_kv_verification_gb300 import build
+    from sparse_kv_verification_gb300 import inputs as I
+    from sparse_kv_verification_gb300 import native as N
+    from sparse_kv_verification_gb300 import replicas as R
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    build.build()
+    N.load()
+    rank, local, world = R.env_rank()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    R.init("nccl")
+
+    wl = I.WORKLOADS[args.config]
+    if args.batch:
+        wl = wl.replace(b=args.batch)
+    n_layers = args.layers or wl.layers
+    rep = Replica(wl, dev, n_layers)
+    L = rep.L
+    K, W = args.steps, max(3, args.warmup)
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(W):
+        rep.step()
+    torch.cuda.synchronize(dev)
+
+    # ---- timed region: K steps, per-phase events on the launch stream.
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4 + 2 * L)]
+           for _ in range(K)]
+    start, end = (torch.cuda.Event(enable_timing=True),
+                  torch.cuda.Event(enable_timing=True))
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    R.barrier(dev)
+    torch.cuda.synchronize(dev)
+    launches0 = N.dustin_launch_count()
+    start.record(stream)
+    for i in range(K):
+        rep.step(evs[i])
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    launches = N.dustin_launch_count() - launches0
+    R.barrier(dev)
+    clock_info = clocks.stop()
+    t_ms = R.reduce_max(start.elapsed_time(end) / K, dev)
+
+    def avg(a, b):
+        return statistics.mean(evs[i][a].elapsed_time(evs[i][b])
+                               for i in range(K)) * 1e3   # us
+    t_score_t = avg(0, 1)
+    t_score_d = avg(1, 2)
+    t_select = avg(2, 3)
+    attn_us = [evs[i][4 + 2 * l].elapsed_time(evs[i][5 + 2 * l]) * 1e3
+               for i in range(K) for l in range(L)]
+    t_attn = statistics.mean(attn_us)
+
+    tokens = wl.b * wl.w * L
+    value = R.reduce_sum(tokens, dev) / (t_ms * 1e-3)
+    peak, peak_kind = measured_peak_gbs()
+    b_attn = rep.bytes_sparse_launch()
+    achieved = b_attn / (t_attn * 1e-6) / 1e9
+
+    # ---- dense in-run baseline: every layer over the full cache.
+    dense = None
+    if not args.no_dense:
+        for full in rep.full[:2]:
+            full()
+        torch.cuda.synchronize(dev)
+        ds = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * L)]
+              for _ in range(args.dense_steps)]
+        for i in range(args.dense_steps):
+            for l, full in enumerate(rep.full):
+                ds[i][2 * l].record()
+                full()
+                ds[i][2 * l + 1].record()
+        torch.cuda.synchronize(dev)
+        per = [ds[i][2 * l].elapsed_time(ds[i][2 * l + 1]) * 1e3
+               for i in range(args.dense_steps) for l in range(L)]
+        t_dense = statistics.mean(per)
+        b_dense = rep.bytes_dense_launch()
+        dense = {"us_per_layer": t_dense,
+                 "hbm_gbs": b_dense / (t_dense * 1e-6) / 1e9,
+                 "frac_of_peak": b_dense / (t_dense * 1e-6) / 1e9 / peak,
+                 "ms_per_step_80_layers": t_dense * L / 1e3,
+                 "speedup_attention_per_layer": t_dense / t_attn,
+                 "speedup_step": t_dense * L / 1e3 / t_ms}
+
+    # ---- end to end: queries from pinned host memory in, outputs out.
+    e2e = None
+    if not args.no_e2e:
+        inp = rep.inp
+        h_in = [t.cpu().pin_memory() for t in ([inp.q_t, inp.q_d] + inp.q)]
+        d_in = [inp.q_t, inp.q_d] + inp.q
+        d_out = rep.o + rep.lse + [rep.idx]
+        h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                 for t in d_out]
+        h2d = sum(t.numel() * t.element_size() for t in h_in)
+        d2h = sum(t.numel() * t.element_size() for t in h_out)
+
+        def e2e_step():
+            for h, d in zip(h_in, d_in):
+                d.copy_(h, non_blocking=True)
+            rep.step()
+            for d, h in zip(d_out, h_out):
+                h.copy_(d, non_blocking=True)
+        for _ in range(W):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        R.barrier(dev)
+        e0, e1 = (torch.cuda.Event(enable_timing=True),
+                  torch.cuda.Event(enable_timing=True))
+        e0.record(stream)
+        for _ in range(K):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        t_e2e = R.reduce_max(e0.elapsed_time(e1) / K, dev)
+        e2e = {"value": R.reduce_sum(tokens, dev) / (t_e2e * 1e-3),
+               "unit": UNIT, "ms_per_step": t_e2e,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        res = run_oracle_leg(args, args.cpu_reps, 1)
+        cpu = {"value": res["value"], "unit": UNIT, "cores": res["cores"],
+               "kind": "oracle", "sample": res["sample"],
+               "wall_s": res["wall_s"]}
+
+    kernels = {
+        "score_target_us": t_score_t,
+        "score_draft_us": t_score_d,
+        "select_us": t_select,
+        "sparse_attn_us_per_layer": t_attn,
+        "score_target_gbs": rep.bytes_score_t() / (t_score_t * 1e-6) / 1e9,
+        "score_draft_gbs": rep.bytes_score_d() / (t_score_d * 1e-6) / 1e9,
+        "sparse_attn_gbs": achieved,
+    }
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": t_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(wl, L),
+        "roofline": {"bound": "hbm", "kernel": "verify_attn_kernel (sparse)",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak,
+                     "peak_kind": f"{peak_kind} hbm_gbs",
+                     "algorithmic_bytes_per_launch": b_attn,
+                     "traffic": committed_traffic()},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+        "clocks": clock_info, "kernels": kernels, "dense": dense,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    R.barrier(dev)
+    R.shutdown()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.oracle_worker:
+        oracle_worker(args)
+        return 0
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -45,6 +45,21 @@ int sm_count() {
   return sms > 0 ? sms : 1;
 }
 
+// Resident CTAs of the (non-paged) attention kernel times the SM count,
+// cached per device, kernel family, head dim and row tile count.
+int attn_slots(bool dense, int d, int mt) {
+  static std::atomic<int> cache[64][2][2][5];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  std::atomic<int>& c = cache[dev][dense ? 1 : 0][d == 128 ? 1 : 0][mt];
+  int v = c.load(std::memory_order_relaxed);
+  if (v > 0) return v;
+  const int occ = dense ? occupancy_attn_dense(d, mt) : occupancy_attn_sparse(d, mt);
+  v = sm_count() * (occ > 0 ? occ : 1);
+  c.store(v, std::memory_order_relaxed);
+  return v;
+}
+
 KvView to_view(const dustin_kv& kv) {
   KvView v;
   v.k = static_cast<const __nv_bfloat16*>(kv.k);
@@ -112,9 +127,7 @@ AttnPlan plan_attn(bool dense, int b, int hq, int hkv, int d, int w, int npos) {
     p.splits = 1;
     p.chunk = 64;
   } else {
-    const int occ = dense ? occupancy_attn_dense(d, p.mt)
-                          : occupancy_attn_sparse(d, p.mt);
-    const long long slots = (long long)sm_count() * occ;
+    const long long slots = (long long)attn_slots(dense, d, p.mt);
     long long s = units >= slots ? 1 : slots / units;
     s = std::min<long long>(s, tiles);
     long long ct = (tiles + s - 1) / s;

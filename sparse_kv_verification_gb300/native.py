@@ -264,3 +264,69 @@ def dustin_device_status() -> int:
 
 def dustin_launch_count() -> int:
     return int(load().dustin_launch_count())
+
+
+# ------------------------------------------------------------------ prepared
+# Pre-marshalled calls for timing loops: every argument (device pointers,
+# descriptors, workspace, stream) is fixed once, so a call is one ctypes
+# dispatch.  The tensors passed in must outlive the returned callable.
+
+def prepare_score_heads(q, kvs, kv_heads, scale, s_out, ws, n, stream=None):
+    _need_cuda(q, s_out, ws)
+    n_pairs, b, rows, d = q.shape
+    arr = (DustinKV * n_pairs)(*kvs)
+    heads = (ctypes.c_int32 * n_pairs)(*[int(h) for h in kv_heads])
+    fn = load().dustin_score_heads
+    args = (b, n, d, n_pairs, rows, q.data_ptr(), ctypes.addressof(arr),
+            ctypes.addressof(heads), float(scale), s_out.data_ptr(),
+            ws.data_ptr(), ws.numel(), _stream(stream, q.device))
+
+    def call():
+        _check(fn(*args))
+    call.keep = (arr, heads)
+    return call
+
+
+def prepare_hybrid_topk(s_draft, s_target, k, n_sink, n_recent, alpha, m,
+                        norm, idx, stream=None):
+    ref = s_draft if s_draft is not None else s_target
+    b, n = ref.shape
+    fn = load().dustin_hybrid_topk
+    args = (b, n, k, n_sink, n_recent, float(alpha), m, norm, _ptr(s_draft),
+            _ptr(s_target), idx.data_ptr(), _stream(stream, ref.device))
+
+    def call():
+        _check(fn(*args))
+    return call
+
+
+def prepare_sparse_verify_attn(q, kv, h_kv, n, idx, scale, o, lse, ws,
+                               stream=None):
+    _attn_checks(q, o, lse)
+    b, h_q, w, d = q.shape
+    fn = load().dustin_sparse_verify_attn
+    kvc = DustinKV.from_buffer_copy(kv)
+    args = (b, h_q, h_kv, d, w, n, idx.shape[1], q.data_ptr(),
+            ctypes.addressof(kvc), idx.data_ptr(), float(scale), o.data_ptr(),
+            lse.data_ptr(), _ptr(ws), 0 if ws is None else ws.numel(),
+            _stream(stream, q.device))
+
+    def call():
+        _check(fn(*args))
+    call.keep = kvc
+    return call
+
+
+def prepare_full_verify_attn(q, kv, h_kv, n, scale, o, lse, ws, stream=None):
+    _attn_checks(q, o, lse)
+    b, h_q, w, d = q.shape
+    fn = load().dustin_full_verify_attn
+    kvc = DustinKV.from_buffer_copy(kv)
+    args = (b, h_q, h_kv, d, w, n, q.data_ptr(), ctypes.addressof(kvc),
+            float(scale), o.data_ptr(), lse.data_ptr(), _ptr(ws),
+            0 if ws is None else ws.numel(), _stream(stream, q.device))
+
+    def call():
+        _check(fn(*args))
+    call.keep = kvc
+    return call

@@ -62,6 +62,8 @@ def parse_args(argv=None):
     p.add_argument("--cpu-rows", type=int, default=1)
     p.add_argument("--cpu-layers", type=int, default=2)
     p.add_argument("--cpu-reps", type=int, default=2)
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="approximate CPU work of the oracle leg")
     p.add_argument("--oracle-worker", action="store_true",
                    help=argparse.SUPPRESS)
     return p.parse_args(argv)
@@ -279,7 +281,13 @@ def oracle_worker(args):
     k_d = [f(k[:, h]) for k, h in zip(inp.k_d, inp.kvh_d)]
     layers = [(f(q), f(k), f(v)) for q, k, v in zip(inp.q, inp.k, inp.v)]
     times = []
-    for _ in range(args.warmup + args.cpu_reps):
+    t_begin = time.perf_counter()
+    reps = 0
+    # Time-bounded: at least cpu_reps repetitions and about min_seconds of
+    # oracle work (capped at 200 repetitions).
+    while reps < args.warmup + args.cpu_reps or (
+            time.perf_counter() - t_begin < args.cpu_seconds and reps < 200):
+        reps += 1
         t0 = time.perf_counter()
         s_t = O.score_heads(q_t, k_t, sample.scale)
         s_d = O.score_heads(q_d, k_d, sample.draft_scale)
@@ -292,7 +300,7 @@ def oracle_worker(args):
             O.verify_attention(q, k, v, idx, sample.scale)
         t3 = time.perf_counter()
         times.append((t1 - t0, t2 - t1, (t3 - t2) / len(layers)))
-    times = times[args.warmup:]
+    times = times[min(args.warmup, len(times) - 1):]
     t_score = statistics.median(t[0] for t in times)
     t_sel = statistics.median(t[1] for t in times)
     t_attn = statistics.median(t[2] for t in times)
@@ -303,7 +311,7 @@ def oracle_worker(args):
         "t_select_s": t_sel, "t_attn_layer_s": t_attn,
         "wall_s": sum(sum(t[:2]) + t[2] * len(layers) for t in times),
         "sample": (f"{sample.b} of {wl.b} sequences, {len(layers)} of "
-                   f"{full_layers} layers timed ({args.cpu_reps} reps, median),"
+                   f"{full_layers} layers timed ({len(times)} reps, median),"
                    f" attention extrapolated to {full_layers} layers; "
                    "single-threaded numpy fp64")}))
 
@@ -314,7 +322,7 @@ def run_oracle_leg(args, reps, warmup):
     cmd = [sys.executable, os.path.abspath(__file__), "--oracle-worker",
            "--config", args.config, "--cpu-rows", str(args.cpu_rows),
            "--cpu-layers", str(args.cpu_layers), "--cpu-reps", str(reps),
-           "--warmup", str(warmup)]
+           "--warmup", str(warmup), "--cpu-seconds", str(args.cpu_seconds)]
     if args.batch:
         cmd += ["--batch", str(args.batch)]
     r = subprocess.run(cmd, capture_output=True, text=True, env=env)

@@ -29,7 +29,9 @@
  *     ABI and no kernel traps.
  *   - Device-side checks (an index >= n, a page id outside the pool) never
  *     fault: the offending position is left out of the attention and a flag
- *     is raised, read with dustin_device_status().
+ *     is raised, read with dustin_device_status().  Every wait inside a
+ *     kernel is bounded (about one second); one that gives up raises
+ *     DUSTIN_DEVFLAG_WAIT_TIMEOUT and the kernel returns.
  *   - Grouped-query attention: query head h reads kv head h / (h_q / h_kv).
  */
 #ifndef DUSTIN_H_
@@ -56,6 +58,8 @@ typedef enum dustin_status {
 /* Device-side flags reported by dustin_device_status(). */
 #define DUSTIN_DEVFLAG_INDEX_RANGE 0x1u /* idx[b][i] < 0 or >= n            */
 #define DUSTIN_DEVFLAG_PAGE_RANGE 0x2u  /* page id < 0 or >= num_pages      */
+#define DUSTIN_DEVFLAG_WAIT_TIMEOUT 0x4u /* a pipeline wait gave up (~1 s);
+                                            the outputs of that call are void */
 
 #define DUSTIN_NORM_NONE 0 /* hybrid mix of the raw score vectors          */
 #define DUSTIN_NORM_L1 1   /* each score vector divided by its own sum     */

@@ -7,13 +7,35 @@
 // rows each: a contiguous [G*w][d] block of q) against a contiguous range
 // of the unit's positions.  Positions are idx[b][i] (sparse) or i (dense).
 //
-// Pipeline: K and V rows of 64-position tiles are gathered with 16-byte
-// cp.async into XOR-swizzled shared memory, STAGES tiles deep.  Warp
-// (wm, wn) owns query rows [16 wm, 16 wm + 16) and a 64/WN-position slice of
-// every tile: S = Q K^T and O += P V run on bf16 mma.sync m16n8k16 with
-// fp32 accumulators, with an online (base-2) softmax in registers.  At the
-// end the WN slices are merged through shared memory; a single split writes
-// O (bf16) and LSE directly, several splits write fp32 partials that
+// Warp-specialised pipeline:
+//  * a producer warpgroup (4 warps) gathers each 64-position tile, 16 rows
+//    per warp: one warp instruction of 16-byte cp.async copies a whole K row
+//    and V row (d = 128; two rows for d = 64) into padded shared-memory rows
+//    (2*d + 16 bytes, so
+//    ldmatrix of eight rows is conflict-free).  Each producer thread then
+//    arms cp.async.mbarrier.arrive on the stage's "full" mbarrier, and lane 0
+//    publishes the warp's 32-row valid mask with a plain (release) arrive.
+//    Row offsets come from a shared-memory table that every thread of the CTA
+//    fills once from idx (and the page table) before the pipeline starts, so
+//    no global-load latency sits inside the producer loop.
+//    Rows that fail a check, and rows past the range, are zero-filled by the
+//    copy (source size 0) and left out through the valid mask.  (Measured on
+//    a 72B-shaped gather of 256-byte rows: 16-byte cp.async reaches 4.3, 5.0
+//    and 5.2 TB/s with 2, 4 and 8 producer warps, per-row TMA bulk copies
+//    1.1 TB/s and TMA tile::gather4 1.8 TB/s, so cp.async does the gather.)
+//    With 16 warps (three consumer warpgroups) the producers hand registers
+//    to the consumers with setmaxnreg (40 / 152 of a 128-register launch).
+//  * MT*WN consumer warps: warp (wm, wn) owns query rows [16 wm, 16 wm + 16)
+//    and a 64/WN-position slice of every tile.  S = Q K^T and O += P V run on
+//    bf16 mma.sync m16n8k16 with fp32 accumulators; the softmax is online in
+//    base 2 with a lazy reference maximum (O and l are rescaled only when a
+//    row maximum grows by more than 2^8), which is exact: the reference only
+//    has to bound the exponents.  Consumers release a stage through its
+//    "empty" mbarrier.
+// STAGES tiles are in flight.  Every mbarrier wait is bounded (about one
+// second): on timeout the kernel raises a flag and winds down.  At the end
+// the WN position slices are merged through shared memory; a single split
+// writes O (bf16) and LSE directly, several splits write fp32 partials that
 // attn_combine_kernel merges.
 #pragma once
 
@@ -41,27 +63,43 @@ struct AttnArgs {
 
 template <int D, int MT>
 struct AttnCfg {
-  static constexpr int WN = (MT == 1) ? 4 : 2;
-  static constexpr int NWARP = MT * WN;
-  static constexpr int NT = NWARP * 32;
+  static constexpr int WN = (MT == 4) ? 2 : 4;
+  static constexpr int NCW = MT * WN;            // consumer warps
+  static constexpr int NPW = 4;                  // producer warps (1 group)
+  static constexpr int NT = (NCW + NPW) * 32;
+  static constexpr int RPW = 64 / NPW;           // tile rows per producer warp
+  // 16 warps run at 128 registers a thread; the producer warpgroup drops to
+  // 40 and the consumer warpgroups rise to 152: 40*128 + 152*384 <= 128*512.
+  static constexpr bool REBALANCE = (NT == 512);
+  static constexpr int PRODUCER_REGS = 40;
+  static constexpr int CONSUMER_REGS = 152;
   static constexpr int TILE = 64;
-  static constexpr int PW = TILE / WN;   // positions per warp per tile
-  static constexpr int NT8 = PW / 8;     // n8 tiles of S per warp
-  static constexpr int KS = D / 16;      // k16 steps over d
-  static constexpr int DT = D / 8;       // n8 tiles of O over d
-  static constexpr int CPR = D / 8;      // 16-byte chunks per row
+  static constexpr int PW = TILE / WN;           // positions per warp per tile
+  static constexpr int NT8 = PW / 8;             // n8 tiles of S per warp
+  static constexpr int KS = D / 16;              // k16 steps over d
+  static constexpr int DT = D / 8;               // n8 tiles of O over d
+  static constexpr int CPR = D / 8;              // 16-byte chunks per row
   static constexpr int ROWS = 16 * MT;
-  static constexpr int STAGES = 4;
-  static constexpr int TILE_BYTES = TILE * D * 2;
-  static constexpr int Q_BYTES = ROWS * D * 2;
-  static constexpr int MAX_TAB = 2048;   // offset-table entries
-  static constexpr int SMEM = Q_BYTES + 2 * STAGES * TILE_BYTES + MAX_TAB * 8;
+  static constexpr int RS = D * 2 + 16;          // padded row stride, bytes
+  static constexpr int STAGES = (D == 128) ? 5 : 8;
+  static constexpr int TILE_BYTES = TILE * RS;
+  static constexpr int Q_BYTES = ROWS * RS;
+  static constexpr int OFF_K = Q_BYTES;
+  static constexpr int OFF_V = OFF_K + STAGES * TILE_BYTES;
+  static constexpr int OFF_MASK = OFF_V + STAGES * TILE_BYTES;
+  static constexpr int OFF_BAR = OFF_MASK + STAGES * NPW * 4;
+  static constexpr int MAX_TAB = 2048;          // offset-table entries
+  static constexpr int OFF_TAB = OFF_BAR + 2 * STAGES * 8;
+  static constexpr int SMEM = OFF_TAB + MAX_TAB * 8;
   static constexpr int MERGE_FLOATS = (WN - 1) * MT * 32 * (DT * 4 + 4);
-  static_assert(MERGE_FLOATS * 4 <= STAGES * TILE_BYTES, "merge buffer");
+  static_assert(MERGE_FLOATS * 4 <= 2 * STAGES * TILE_BYTES, "merge buffer");
+  static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
 // Device-side check flags of this translation unit.
 static __device__ unsigned int g_attn_dev_flags;
+
+constexpr float kLazyRescale = 8.0f;  // log2 units
 
 template <int D, int MT, bool PAGED, bool DENSE>
 __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
@@ -69,15 +107,17 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
   using C = AttnCfg<D, MT>;
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* sQ = smem;
-  unsigned char* sK = sQ + C::Q_BYTES;
-  unsigned char* sV = sK + C::STAGES * C::TILE_BYTES;
-  long long* tab = reinterpret_cast<long long*>(sV + C::STAGES * C::TILE_BYTES);
+  unsigned char* sK = smem + C::OFF_K;
+  unsigned char* sV = smem + C::OFF_V;
+  unsigned* sMask = reinterpret_cast<unsigned*>(smem + C::OFF_MASK);
+  long long* tab = reinterpret_cast<long long*>(smem + C::OFF_TAB);
+  const uint32_t bar0 = smem_u32(smem + C::OFF_BAR);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
-  const int wm = warp / C::WN;
-  const int wn = warp % C::WN;
 
   // Block -> (b, kv head, row block, split).
   int blk = blockIdx.x;
@@ -96,35 +136,41 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
   const long long unit_off = (long long)bb * a.kv.sb + (long long)g * a.kv.sh;
   const long long row_base =
       ((long long)bb * a.hq + (long long)g * a.group) * a.w;  // first q row
-  const int r_lo = rb * C::ROWS;                               // first row here
+  const int r_lo = rb * C::ROWS;
 
-  // ---- Q rows into shared memory (zero rows past G*w).
+  // ---- Q rows into shared memory (zero rows past G*w), barriers.
   for (int c = tid; c < C::ROWS * C::CPR; c += C::NT) {
     const int r = c / C::CPR, ch = c % C::CPR;
     const int R = r_lo + r;
     const bool ok = R < a.rows;
-    const __nv_bfloat16* src = a.q + (ok ? (row_base + R) * D + ch * 8 : 0);
-    cp_async_16(smem_u32(sQ + swz<D>(r, ch)), src, ok ? 16 : 0);
+    cp_async_16(smem_u32(sQ + r * C::RS + ch * 16),
+                a.q + (ok ? (row_base + R) * D + ch * 8 : 0), ok ? 16 : 0);
   }
   cp_async_commit();
-
-  // ---- Offset table: element offset of each position's K/V row (sparse),
-  // or of each page (dense, paged).  -1 marks a position that failed a check.
+  if (tid == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(full_bar(s), C::NPW * 32 + C::NPW);  // copies + mask arrives
+      mbar_init(empty_bar(s), C::NCW);
+    }
+    mbar_fence_init();
+  }
+  // Offset table: element offset of each position's K/V row (sparse), or of
+  // each page (dense, paged); -1 marks a row that failed a check.
   if constexpr (!DENSE) {
+    const int* idx_row = a.idx + (long long)bb * a.npos + p_begin;
     for (int i = tid; i < len; i += C::NT) {
-      const int j = __ldg(a.idx + (long long)bb * a.npos + p_begin + i);
+      const int j = __ldg(idx_row + i);
       long long off = -1;
       if (j < 0 || j >= a.n) {
         atomicOr(&g_attn_dev_flags, 1u);
       } else if constexpr (PAGED) {
-        const int pg = __ldg(a.kv.page_table + (long long)bb * a.kv.pages_per_seq +
-                             j / a.kv.page_size);
-        if (pg < 0 || pg >= a.kv.num_pages) {
+        const int pg = __ldg(a.kv.page_table +
+                             (long long)bb * a.kv.pages_per_seq + j / a.kv.page_size);
+        if (pg < 0 || pg >= a.kv.num_pages)
           atomicOr(&g_attn_dev_flags, 2u);
-        } else {
+        else
           off = (long long)pg * a.kv.sb + (long long)g * a.kv.sh +
                 (long long)(j % a.kv.page_size) * a.kv.sn;
-        }
       } else {
         off = unit_off + (long long)j * a.kv.sn;
       }
@@ -137,58 +183,90 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
       const int pg = __ldg(a.kv.page_table + (long long)bb * a.kv.pages_per_seq +
                            pg0 + i);
       long long off = -1;
-      if (pg < 0 || pg >= a.kv.num_pages) {
+      if (pg < 0 || pg >= a.kv.num_pages)
         atomicOr(&g_attn_dev_flags, 2u);
-      } else {
+      else
         off = (long long)pg * a.kv.sb + (long long)g * a.kv.sh;
-      }
       tab[i] = off;
     }
   }
+  cp_async_wait<0>();
   __syncthreads();
 
-  auto row_offset = [&](int i) -> long long {
-    if constexpr (!DENSE) {
-      return tab[i];
-    } else if constexpr (PAGED) {
-      const int j = p_begin + i;
-      const long long base = tab[j / a.kv.page_size - p_begin / a.kv.page_size];
-      return base < 0 ? -1 : base + (long long)(j % a.kv.page_size) * a.kv.sn;
-    } else {
-      return unit_off + (long long)(p_begin + i) * a.kv.sn;
-    }
-  };
+  if (warp >= C::NCW) {
+    // =========================== producer warps ==========================
+    // Warp pw fetches rows [RPW pw, RPW pw + RPW) of every tile.  Lane l
+    // looks up the offset of row RPW pw + l % RPW (-1: leave the row out);
+    // the copies of row rr use lane rr's offset through a shuffle.
+    if constexpr (C::REBALANCE)
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(C::PRODUCER_REGS));
+    const int pw = warp - C::NCW;
+    const int my_row = pw * C::RPW + (lane % C::RPW);
+    constexpr int LPR = 2 * C::CPR;   // lanes per row: K chunks, then V chunks
+    constexpr int RPI = 32 / LPR;     // rows per warp instruction
+    const int sub = lane / LPR;
+    const int l2 = lane % LPR;
+    const bool is_v = l2 >= C::CPR;
+    const int ch = l2 % C::CPR;
+    const __nv_bfloat16* src_base = is_v ? a.kv.v : a.kv.k;
+    unsigned char* dst_base = is_v ? sV : sK;
 
-  auto issue_tile = [&](int t) {
-    if (t < ntiles) {
-      const int stage = t % C::STAGES;
-      const uint32_t dk = smem_u32(sK + stage * C::TILE_BYTES);
-      const uint32_t dv = smem_u32(sV + stage * C::TILE_BYTES);
-      for (int c = tid; c < C::TILE * C::CPR; c += C::NT) {
-        const int r = c / C::CPR, ch = c % C::CPR;
-        const int i = t * C::TILE + r;
-        long long off = (i < len) ? row_offset(i) : -1;
+    auto row_offset = [&](int t) -> long long {  // -1: leave the row out
+      const int i = t * C::TILE + my_row;
+      if (i >= len) return -1;
+      if constexpr (!DENSE) {
+        return tab[i];
+      } else if constexpr (PAGED) {
+        const int j = p_begin + i;
+        const long long base = tab[j / a.kv.page_size - p_begin / a.kv.page_size];
+        return base < 0 ? -1 : base + (long long)(j % a.kv.page_size) * a.kv.sn;
+      } else {
+        return unit_off + (long long)(p_begin + i) * a.kv.sn;
+      }
+    };
+
+    for (int t = 0; t < ntiles; ++t) {
+      const int s = t % C::STAGES;
+      if (t >= C::STAGES &&
+          !mbar_wait(empty_bar(s), ((t / C::STAGES) & 1) ^ 1, kWaitLimitCycles)) {
+        if (lane == 0) atomicOr(&g_attn_dev_flags, 4u);
+        break;
+      }
+      const long long my_off = row_offset(t);
+      const unsigned vm = __ballot_sync(0xffffffffu, my_off >= 0) &
+                          (C::RPW == 32 ? 0xffffffffu : ((1u << C::RPW) - 1u));
+      unsigned char* dst = dst_base + s * C::TILE_BYTES + ch * 16;
+#pragma unroll 4
+      for (int it = 0; it < C::RPW / RPI; ++it) {
+        const int rr = it * RPI + sub;
+        const long long off = __shfl_sync(0xffffffffu, my_off, rr);
         const bool ok = off >= 0;
-        const long long e = ok ? off + ch * 8 : 0;
-        cp_async_16(dk + swz<D>(r, ch), a.kv.k + e, ok ? 16 : 0);
-        cp_async_16(dv + swz<D>(r, ch), a.kv.v + e, ok ? 16 : 0);
+        cp_async_16(smem_u32(dst + (pw * C::RPW + rr) * C::RS),
+                    src_base + (ok ? off + ch * 8 : 0), ok ? 16 : 0);
+      }
+      cp_async_mbar_arrive(full_bar(s));
+      if (lane == 0) {
+        sMask[s * C::NPW + pw] = vm;
+        mbar_arrive(full_bar(s));
       }
     }
-    cp_async_commit();
-  };
+    // Every copy of this thread lands before the CTA may exit.
+    cp_async_wait<0>();
+    return;
+  }
 
-  for (int t = 0; t < C::STAGES - 1; ++t) issue_tile(t);
-
-  // ---- Q fragments (A operand) into registers.
-  cp_async_wait<C::STAGES - 1>();  // the Q group is the oldest
-  __syncthreads();
+  // ============================ consumer warps ============================
+  if constexpr (C::REBALANCE)
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(C::CONSUMER_REGS));
+  const int wm = warp / C::WN;
+  const int wn = warp % C::WN;
   uint32_t qf[C::KS][4];
 #pragma unroll
   for (int ks = 0; ks < C::KS; ++ks) {
     const int r = wm * 16 + (lane & 15);
     const int ch = ks * 2 + (lane >> 4);
-    ldmatrix_x4(smem_u32(sQ + swz<D>(r, ch)), qf[ks][0], qf[ks][1], qf[ks][2],
-                qf[ks][3]);
+    ldmatrix_x4(smem_u32(sQ + r * C::RS + ch * 16), qf[ks][0], qf[ks][1],
+                qf[ks][2], qf[ks][3]);
   }
 
   float oacc[C::DT][4];
@@ -197,24 +275,27 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
 #pragma unroll
     for (int e = 0; e < 4; ++e) oacc[i][e] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-
   const int gq = lane >> 2, tq = lane & 3;
 
   for (int t = 0; t < ntiles; ++t) {
-    cp_async_wait<C::STAGES - 2>();
-    __syncthreads();
-    issue_tile(t + C::STAGES - 1);
-
-    const int stage = t % C::STAGES;
-    const unsigned char* tk = sK + stage * C::TILE_BYTES;
-    const unsigned char* tv = sV + stage * C::TILE_BYTES;
+    const int s = t % C::STAGES;
+    if (!mbar_wait(full_bar(s), (t / C::STAGES) & 1, kWaitLimitCycles)) {
+      if (lane == 0) atomicOr(&g_attn_dev_flags, 4u);
+      break;
+    }
+    const unsigned char* tk = sK + s * C::TILE_BYTES;
+    const unsigned char* tv = sV + s * C::TILE_BYTES;
+    unsigned long long vmask = 0;
+#pragma unroll
+    for (int p = 0; p < C::NPW; ++p)
+      vmask |= (unsigned long long)sMask[s * C::NPW + p] << (p * C::RPW);
 
     // S = Q K^T over this warp's PW positions.
-    float s[C::NT8][4];
+    float sc[C::NT8][4];
 #pragma unroll
     for (int j = 0; j < C::NT8; ++j)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) s[j][e] = 0.f;
+      for (int e = 0; e < 4; ++e) sc[j][e] = 0.f;
 #pragma unroll
     for (int ks = 0; ks < C::KS; ++ks) {
 #pragma unroll
@@ -222,76 +303,90 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
         const int r = wn * C::PW + j * 8 + ((lane >> 4) << 3) + (lane & 7);
         const int ch = ks * 2 + ((lane >> 3) & 1);
         uint32_t b0, b1, b2, b3;
-        ldmatrix_x4(smem_u32(tk + swz<D>(r, ch)), b0, b1, b2, b3);
-        mma_bf16(s[j], qf[ks], b0, b1);
-        mma_bf16(s[j + 1], qf[ks], b2, b3);
+        ldmatrix_x4(smem_u32(tk + r * C::RS + ch * 16), b0, b1, b2, b3);
+        mma_bf16(sc[j], qf[ks], b0, b1);
+        mma_bf16(sc[j + 1], qf[ks], b2, b3);
       }
     }
 
-    // Scale into log2 units, mask positions past the range or failed checks.
+    // Scale into log2 units; rows left out of the tile get -inf.
     float mx0 = -INFINITY, mx1 = -INFINITY;
+    if (vmask == ~0ull) {
+#pragma unroll
+      for (int j = 0; j < C::NT8; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[j][e] *= a.scale_log2;
+    } else {
+#pragma unroll
+      for (int j = 0; j < C::NT8; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int pos = wn * C::PW + j * 8 + 2 * tq + e;
+          const bool ok = (vmask >> pos) & 1ull;
+          sc[j][e] = ok ? sc[j][e] * a.scale_log2 : -INFINITY;
+          sc[j][e + 2] = ok ? sc[j][e + 2] * a.scale_log2 : -INFINITY;
+        }
+    }
 #pragma unroll
     for (int j = 0; j < C::NT8; ++j) {
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int i = t * C::TILE + wn * C::PW + j * 8 + 2 * tq + e;
-        bool ok = i < len;
-        if constexpr (!DENSE) ok = ok && tab[i] >= 0;
-        if constexpr (DENSE && PAGED) ok = ok && row_offset(i) >= 0;
-        s[j][e] = ok ? s[j][e] * a.scale_log2 : -INFINITY;
-        s[j][e + 2] = ok ? s[j][e + 2] * a.scale_log2 : -INFINITY;
-        mx0 = fmaxf(mx0, s[j][e]);
-        mx1 = fmaxf(mx1, s[j][e + 2]);
-      }
+      mx0 = fmaxf(mx0, fmaxf(sc[j][0], sc[j][1]));
+      mx1 = fmaxf(mx1, fmaxf(sc[j][2], sc[j][3]));
     }
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-    const float u0 = (n0 == -INFINITY) ? 0.f : n0;   // subtrahend
-    const float u1 = (n1 == -INFINITY) ? 0.f : n1;
-    const float c0 = ex2(m0 - u0), c1 = ex2(m1 - u1);
-    m0 = n0;
-    m1 = n1;
-    float ps0 = 0.f, ps1 = 0.f;
+    // Lazy rescale: move a row's reference maximum only when the tile's
+    // maximum exceeds it by more than 2^kLazyRescale.
+    const bool up0 = mx0 > m0 + kLazyRescale, up1 = mx1 > m1 + kLazyRescale;
+    if (__any_sync(0xffffffffu, up0 || up1)) {
+      const float n0 = up0 ? mx0 : m0, n1 = up1 ? mx1 : m1;
+      const float c0 = up0 ? ex2(m0 - n0) : 1.f;   // ex2(-inf) = 0
+      const float c1 = up1 ? ex2(m1 - n1) : 1.f;
+      m0 = n0;
+      m1 = n1;
+      l0 *= c0;
+      l1 *= c1;
+#pragma unroll
+      for (int dt = 0; dt < C::DT; ++dt) {
+        oacc[dt][0] *= c0;
+        oacc[dt][1] *= c0;
+        oacc[dt][2] *= c1;
+        oacc[dt][3] *= c1;
+      }
+    }
+    const float u0 = (m0 == -INFINITY) ? 0.f : m0;
+    const float u1 = (m1 == -INFINITY) ? 0.f : m1;
 #pragma unroll
     for (int j = 0; j < C::NT8; ++j) {
-      s[j][0] = ex2(s[j][0] - u0);
-      s[j][1] = ex2(s[j][1] - u0);
-      s[j][2] = ex2(s[j][2] - u1);
-      s[j][3] = ex2(s[j][3] - u1);
-      ps0 += s[j][0] + s[j][1];
-      ps1 += s[j][2] + s[j][3];
-    }
-    l0 = l0 * c0 + ps0;
-    l1 = l1 * c1 + ps1;
-#pragma unroll
-    for (int dt = 0; dt < C::DT; ++dt) {
-      oacc[dt][0] *= c0;
-      oacc[dt][1] *= c0;
-      oacc[dt][2] *= c1;
-      oacc[dt][3] *= c1;
+      sc[j][0] = ex2(sc[j][0] - u0);
+      sc[j][1] = ex2(sc[j][1] - u0);
+      sc[j][2] = ex2(sc[j][2] - u1);
+      sc[j][3] = ex2(sc[j][3] - u1);
+      l0 += sc[j][0] + sc[j][1];
+      l1 += sc[j][2] + sc[j][3];
     }
 
     // O += P V.
 #pragma unroll
     for (int kk = 0; kk < C::PW / 16; ++kk) {
       uint32_t pa[4];
-      pa[0] = pack_bf16(s[2 * kk][0], s[2 * kk][1]);
-      pa[1] = pack_bf16(s[2 * kk][2], s[2 * kk][3]);
-      pa[2] = pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-      pa[3] = pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+      pa[0] = pack_bf16(sc[2 * kk][0], sc[2 * kk][1]);
+      pa[1] = pack_bf16(sc[2 * kk][2], sc[2 * kk][3]);
+      pa[2] = pack_bf16(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
+      pa[3] = pack_bf16(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
 #pragma unroll
       for (int dt = 0; dt < C::DT; dt += 2) {
         const int r = wn * C::PW + kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
         const int ch = dt + (lane >> 4);
         uint32_t b0, b1, b2, b3;
-        ldmatrix_x4_trans(smem_u32(tv + swz<D>(r, ch)), b0, b1, b2, b3);
+        ldmatrix_x4_trans(smem_u32(tv + r * C::RS + ch * 16), b0, b1, b2, b3);
         mma_bf16(oacc[dt], pa, b0, b1);
         mma_bf16(oacc[dt + 1], pa, b2, b3);
       }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty_bar(s));
   }
 
   // ---- Row sums over the quad, then merge the WN position slices.
@@ -300,8 +395,8 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
   l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
 
-  cp_async_wait<0>();
-  __syncthreads();
+  // Every issued copy was waited for, so the stages are free to reuse.
+  named_bar_sync(1, C::NCW * 32);
   if constexpr (C::WN > 1) {
     float* mb = reinterpret_cast<float*>(sK);
     constexpr int SLOTS = C::DT * 4 + 4;
@@ -316,7 +411,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e) p[(4 + dt * 4 + e) * 32] = oacc[dt][e];
     }
-    __syncthreads();
+    named_bar_sync(1, C::NCW * 32);
     if (wn == 0) {
 #pragma unroll 1
       for (int o = 1; o < C::WN; ++o) {

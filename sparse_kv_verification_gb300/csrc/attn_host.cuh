@@ -27,9 +27,25 @@ template <bool DENSE>
 struct AttnHost {
   template <int D, int MT, bool PAGED>
   static cudaError_t prepare() {
+    using C = AttnCfg<D, MT>;
     static std::atomic<uint64_t> done{0};
-    return ensure_smem_attr(verify_attn_kernel<D, MT, PAGED, DENSE>,
-                            AttnCfg<D, MT>::SMEM, done);
+    if constexpr (C::REBALANCE) {
+      // setmaxnreg only redistributes the registers the block was launched
+      // with: refuse to launch if the compiled allocation could not cover
+      // the requested split (the increase would otherwise never complete).
+      static std::atomic<int> checked{0};
+      if (checked.load() == 0) {
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, verify_attn_kernel<D, MT, PAGED, DENSE>);
+        if (e != cudaSuccess) return e;
+        const long long have = (long long)fa.numRegs * C::NT;
+        const long long need = (long long)C::PRODUCER_REGS * 128 +
+                               (long long)C::CONSUMER_REGS * (C::NT - 128);
+        checked.store(have >= need ? 1 : -1);
+      }
+      if (checked.load() < 0) return cudaErrorInvalidConfiguration;
+    }
+    return ensure_smem_attr(verify_attn_kernel<D, MT, PAGED, DENSE>, C::SMEM, done);
   }
 
   template <int D, int MT, bool PAGED>

@@ -137,6 +137,34 @@ int dustin_score_heads(int b, int n, int d, int n_pairs, int rows,
                        void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Scoring without a caller-provided workspace.  The paper has no
+ * counterpart: this is a convenience of this library.
+ *
+ * For callers that cannot allocate device memory when they score -- for
+ * example a serving loop that has given all of HBM to the KV cache (a
+ * cudaMalloc there fails or stalls the step), or a plugin whose framework
+ * owns the allocator and hands over only inputs and outputs.  Same inputs,
+ * outputs and limits as dustin_score_heads, but the scratch lives in a fixed
+ * array of DUSTIN_NOALLOC_SCRATCH_BYTES compiled into the library (every GPU
+ * that loads the library keeps it until the process exits).  The call
+ * allocates nothing.
+ *   - A call whose scratch (dustin_score_heads_workspace_size) exceeds the
+ *     array is rejected with DUSTIN_ERR_WORKSPACE before anything runs.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the one array, which keeps the last call's contents.
+ *     Each call overwrites every scratch byte it reads, so nothing needs
+ *     clearing, but calls that overlap on the GPU (other streams, other
+ *     threads) race on the array: serialise them.
+ */
+#define DUSTIN_NOALLOC_SCRATCH_BYTES (64u << 20)
+int dustin_score_heads_noalloc(int b, int n, int d, int n_pairs, int rows,
+                               const void* q, const dustin_kv* kv,
+                               const int32_t* kv_head, float scale,
+                               float* s_out, void* stream);
+
+/* ------------------------------------------------------------------------
  * Hybrid combination and global per-sequence Top-K ([Notes] sections 2.2
  * and 2.3).  One index set per sequence, shared by all layers and heads.
  *

@@ -227,6 +227,10 @@ int run_attn(bool dense, int b, int hq, int hkv, int d, int w, int n, int k,
 
 void note_launches(int count) { g_launches.fetch_add((uint64_t)count); }
 
+int record_error(int status, const char* message) {
+  return fail(status, "%s", message);
+}
+
 }  // namespace dustin
 
 using namespace dustin;

@@ -57,5 +57,6 @@ cudaError_t take_attn_dense_flags(unsigned* flags);
 
 // ---- bookkeeping (api.cu)
 void note_launches(int count);
+int record_error(int status, const char* message);  // sets dustin_last_error()
 
 }  // namespace dustin

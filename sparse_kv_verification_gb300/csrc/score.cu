@@ -13,7 +13,12 @@
 // Pass 2 (score_reduce_kernel): combines the chunk statistics into each
 // row's log2-sum-exp and writes S[b][j] = sum_{p,r} 2^(l - lse2), summed
 // in a fixed order (pair-major, then row) in fp32.
+#include <atomic>
+#include <cstdio>
+#include <mutex>
+
 #include "device_common.cuh"
+#include "dustin.h"
 #include "internal.h"
 
 namespace dustin {
@@ -268,3 +273,80 @@ cudaError_t take_score_flags(unsigned* flags) {
 }
 
 }  // namespace dustin
+
+// ------------------------------------------------------------------------
+// Scoring without a caller-provided workspace.
+//
+// Some callers cannot allocate device memory when they score: a serving
+// loop that has handed all of HBM to the KV cache (cudaMalloc would fail or
+// stall the step), or a plugin whose host framework owns the allocator and
+// passes only input and output buffers.  dustin_score_heads_noalloc gives
+// them the scoring call with its scratch in a fixed array compiled into this
+// library.  Every GPU that loads the library holds the array until the
+// process exits.
+namespace dustin {
+namespace {
+
+static __device__ __align__(256) unsigned char
+    g_noalloc_scratch[DUSTIN_NOALLOC_SCRATCH_BYTES];
+
+std::atomic<void*> g_noalloc_ptr[64];
+std::mutex g_noalloc_mutex;
+
+// Device address of the array on the current device, looked up once per
+// device (with that device current).  In host code the array's name is only
+// a host-side stand-in, so the kernels always get this address.
+cudaError_t noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  void* p = g_noalloc_ptr[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    p = g_noalloc_ptr[dev].load(std::memory_order_acquire);
+    if (p == nullptr) {
+      e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+      if (e != cudaSuccess) return e;
+      g_noalloc_ptr[dev].store(p, std::memory_order_release);
+    }
+  }
+  *out = p;
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace dustin
+
+extern "C" int dustin_score_heads_noalloc(int b, int n, int d, int n_pairs,
+                                          int rows, const void* q,
+                                          const dustin_kv* kv,
+                                          const int32_t* kv_head, float scale,
+                                          float* s_out, void* stream) {
+  using namespace dustin;
+  const size_t need = dustin_score_heads_workspace_size(b, n, n_pairs, rows);
+  if (need > (size_t)DUSTIN_NOALLOC_SCRATCH_BYTES) {
+    char msg[256];
+    snprintf(msg, sizeof(msg),
+             "dustin_score_heads_noalloc: this call needs %zu bytes of scratch; "
+             "the built-in array holds %zu (use dustin_score_heads with a "
+             "workspace)",
+             need, (size_t)DUSTIN_NOALLOC_SCRATCH_BYTES);
+    return record_error(DUSTIN_ERR_WORKSPACE, msg);
+  }
+  if (need == 0)  // empty or invalid sizes: the checks of the main entry point
+    return dustin_score_heads(b, n, d, n_pairs, rows, q, kv, kv_head, scale,
+                              s_out, nullptr, 0, stream);
+  void* ws = nullptr;
+  cudaError_t e = noalloc_scratch(&ws);
+  if (e != cudaSuccess) {
+    char msg[256];
+    snprintf(msg, sizeof(msg),
+             "dustin_score_heads_noalloc: cudaGetSymbolAddress: %s",
+             cudaGetErrorString(e));
+    return record_error(DUSTIN_ERR_CUDA, msg);
+  }
+  return dustin_score_heads(b, n, d, n_pairs, rows, q, kv, kv_head, scale,
+                            s_out, ws, (size_t)DUSTIN_NOALLOC_SCRATCH_BYTES,
+                            stream);
+}

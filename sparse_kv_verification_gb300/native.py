@@ -23,6 +23,7 @@ EXPORTS = (
     "dustin_status_string", "dustin_last_error", "dustin_version",
     "dustin_launch_count", "dustin_device_status",
     "dustin_score_heads_workspace_size", "dustin_score_heads",
+    "dustin_score_heads_noalloc",
     "dustin_hybrid_topk",
     "dustin_sparse_verify_attn_workspace_size", "dustin_sparse_verify_attn",
     "dustin_full_verify_attn_workspace_size", "dustin_full_verify_attn",
@@ -80,6 +81,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         "dustin_device_status": (I, [P]),
         "dustin_score_heads_workspace_size": (S, [I, I, I, I]),
         "dustin_score_heads": (I, [I, I, I, I, I, P, P, P, F, P, P, S, P]),
+        "dustin_score_heads_noalloc": (I, [I, I, I, I, I, P, P, P, F, P, P]),
         "dustin_hybrid_topk": (I, [I, I, I, I, I, D, I, I, P, P, P, P]),
         "dustin_sparse_verify_attn_workspace_size": (S, [I, I, I, I, I, I]),
         "dustin_sparse_verify_attn": (I, [I, I, I, I, I, I, I, P, P, P, F, P, P,
@@ -175,6 +177,30 @@ def dustin_score_heads(q: torch.Tensor, kvs: Sequence[DustinKV],
         b, n, d, n_pairs, rows, q.data_ptr(), ctypes.addressof(arr),
         ctypes.addressof(heads), float(scale), s_out.data_ptr(), ws.data_ptr(),
         ws.numel(), _stream(stream, q.device)))
+
+
+NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def dustin_score_heads_noalloc(q: torch.Tensor, kvs: Sequence[DustinKV],
+                               kv_heads: Sequence[int], scale: float,
+                               s_out: torch.Tensor, n: int,
+                               stream=None) -> None:
+    """dustin_score_heads with the library's built-in scratch array instead
+    of a workspace: for callers that cannot allocate device memory.  Calls
+    share the array and must not overlap on the GPU."""
+    _need_cuda(q, s_out)
+    n_pairs, b, rows, d = q.shape
+    if len(kvs) != n_pairs or len(kv_heads) != n_pairs:
+        raise ValueError("one kv descriptor and kv head per scored pair")
+    if not q.is_contiguous() or s_out.dtype != torch.float32:
+        raise ValueError("q must be contiguous; s_out fp32")
+    arr = (DustinKV * n_pairs)(*kvs)
+    heads = (ctypes.c_int32 * n_pairs)(*[int(h) for h in kv_heads])
+    _check(load().dustin_score_heads_noalloc(
+        b, n, d, n_pairs, rows, q.data_ptr(), ctypes.addressof(arr),
+        ctypes.addressof(heads), float(scale), s_out.data_ptr(),
+        _stream(stream, q.device)))
 
 
 # ------------------------------------------------------------------ selection

@@ -210,7 +210,8 @@ int dustin_hybrid_topk(int b, int n, int k, int n_sink, int n_recent,
  *   o    bf16 [b][h_q][w][d], device;  lse fp32 [b][h_q][w] (natural log)
  *   ws   device scratch of dustin_sparse_verify_attn_workspace_size() bytes
  *        (may be 0 bytes; ws may then be NULL)
- * Limits: d in {64, 128}; h_q a multiple of h_kv; k <= n.
+ * Limits: d in {64, 128}; h_q a multiple of h_kv; k <= n; scale finite and
+ * > 0.
  */
 size_t dustin_sparse_verify_attn_workspace_size(int b, int h_q, int h_kv,
                                                 int d, int w, int k);

@@ -49,16 +49,21 @@ def up_to_date() -> bool:
 
 
 def build(force: bool = False, verbose: bool = False,
-          extra: List[str] | None = None) -> str:
-    """Compiles the library if needed and returns its path."""
-    if not force and up_to_date():
+          extra: List[str] | None = None, out: str | None = None) -> str:
+    """Compiles the library if needed and returns its path.  `extra` adds
+    nvcc flags (e.g. -D tunables); `out` builds to another path (always
+    rebuilt)."""
+    if out is None and not force and up_to_date():
         return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    lib_path = out or LIB
+    obj_dir = os.path.join(os.path.dirname(os.path.abspath(lib_path)),
+                           "obj_" + os.path.basename(lib_path)) if out else BUILD
+    os.makedirs(obj_dir, exist_ok=True)
     cc = nvcc()
     extra = list(extra or [])
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(obj_dir, os.path.splitext(src)[0] + ".o")
         cmd = [cc, *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src),
                "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -70,13 +75,13 @@ def build(force: bool = False, verbose: bool = False,
 
     with concurrent.futures.ThreadPoolExecutor(len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + ".tmp"
+    tmp = lib_path + ".tmp"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -183,8 +183,8 @@ int run_attn(bool dense, int b, int hq, int hkv, int d, int w, int n, int k,
       (idx && (reinterpret_cast<uintptr_t>(idx) & 3u)))
     return fail(DUSTIN_ERR_ALIGNMENT, "%s: q/o need 16-byte, lse/idx 4-byte alignment",
                 what);
-  if (!std::isfinite(scale))
-    return fail(DUSTIN_ERR_INVALID_ARG, "%s: scale is not finite", what);
+  if (!std::isfinite(scale) || !(scale > 0.f))
+    return fail(DUSTIN_ERR_INVALID_ARG, "%s: scale must be finite and > 0", what);
   rc = check_kv(kv, b, n, d, true, what);
   if (rc) return rc;
   const int npos = dense ? n : k;

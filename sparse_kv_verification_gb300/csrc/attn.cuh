@@ -61,18 +61,41 @@ struct AttnArgs {
   float2* ws_ml;    // [blocks][splits][16 MT]    (m in log2 units, l)
 };
 
+// Build-time tunables (nvcc -D): producer warps (4 or 8), pipeline depth
+// for d = 128, and split accumulators for S = Q K^T (two half-depth chains
+// per n8 tile instead of one, for instruction-level parallelism).
+#ifndef DUSTIN_ATTN_NPW
+#define DUSTIN_ATTN_NPW 4
+#endif
+#ifndef DUSTIN_ATTN_STAGES128
+#define DUSTIN_ATTN_STAGES128 5
+#endif
+#ifndef DUSTIN_ATTN_SPLIT_QK
+#define DUSTIN_ATTN_SPLIT_QK 0
+#endif
+#ifndef DUSTIN_ATTN_ROTATE
+#define DUSTIN_ATTN_ROTATE 1
+#endif
+#ifndef DUSTIN_ATTN_PLAIN_CP
+#define DUSTIN_ATTN_PLAIN_CP 0
+#endif
+
 template <int D, int MT>
 struct AttnCfg {
   static constexpr int WN = (MT == 4) ? 2 : 4;
   static constexpr int NCW = MT * WN;            // consumer warps
-  static constexpr int NPW = 4;                  // producer warps (1 group)
+  static constexpr int NPW = DUSTIN_ATTN_NPW;    // producer warps
+  static_assert(NPW == 4 || NPW == 8, "producer warps: whole warpgroups");
   static constexpr int NT = (NCW + NPW) * 32;
   static constexpr int RPW = 64 / NPW;           // tile rows per producer warp
-  // 16 warps run at 128 registers a thread; the producer warpgroup drops to
-  // 40 and the consumer warpgroups rise to 152: 40*128 + 152*384 <= 128*512.
-  static constexpr bool REBALANCE = (NT == 512);
+  // Above 384 threads the register file is tight: the producer warpgroups
+  // drop to 40 registers and the consumer warpgroups take the rest, e.g.
+  // 16 warps (128 at launch): 40*128 + 152*384 <= 128*512.
+  static constexpr bool REBALANCE = (NT > 384);
   static constexpr int PRODUCER_REGS = 40;
-  static constexpr int CONSUMER_REGS = 152;
+  static constexpr int LAUNCH_REGS = (65536 / NT) & ~7;
+  static constexpr int CONSUMER_REGS =
+      ((LAUNCH_REGS * NT - PRODUCER_REGS * NPW * 32) / (NCW * 32)) & ~7;
   static constexpr int TILE = 64;
   static constexpr int PW = TILE / WN;           // positions per warp per tile
   static constexpr int NT8 = PW / 8;             // n8 tiles of S per warp
@@ -81,13 +104,13 @@ struct AttnCfg {
   static constexpr int CPR = D / 8;              // 16-byte chunks per row
   static constexpr int ROWS = 16 * MT;
   static constexpr int RS = D * 2 + 16;          // padded row stride, bytes
-  static constexpr int STAGES = (D == 128) ? 5 : 8;
+  static constexpr int STAGES = (D == 128) ? DUSTIN_ATTN_STAGES128 : 8;
   static constexpr int TILE_BYTES = TILE * RS;
   static constexpr int Q_BYTES = ROWS * RS;
   static constexpr int OFF_K = Q_BYTES;
   static constexpr int OFF_V = OFF_K + STAGES * TILE_BYTES;
   static constexpr int OFF_MASK = OFF_V + STAGES * TILE_BYTES;
-  static constexpr int OFF_BAR = OFF_MASK + STAGES * NPW * 4;
+  static constexpr int OFF_BAR = OFF_MASK + STAGES * 8;   // 64-bit mask / stage
   static constexpr int MAX_TAB = 2048;          // offset-table entries
   static constexpr int OFF_TAB = OFF_BAR + 2 * STAGES * 8;
   static constexpr int SMEM = OFF_TAB + MAX_TAB * 8;
@@ -109,7 +132,8 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
   unsigned char* sQ = smem;
   unsigned char* sK = smem + C::OFF_K;
   unsigned char* sV = smem + C::OFF_V;
-  unsigned* sMask = reinterpret_cast<unsigned*>(smem + C::OFF_MASK);
+  unsigned long long* sMask64 =
+      reinterpret_cast<unsigned long long*>(smem + C::OFF_MASK);
   long long* tab = reinterpret_cast<long long*>(smem + C::OFF_TAB);
   const uint32_t bar0 = smem_u32(smem + C::OFF_BAR);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -134,6 +158,12 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
   const int ntiles = (len + C::TILE - 1) / C::TILE;
 
   const long long unit_off = (long long)bb * a.kv.sb + (long long)g * a.kv.sh;
+  // The kv heads of a sequence share one index set, so their CTAs would
+  // gather the same positions from planes a fixed stride apart at the same
+  // moment.  Each kv head starts at a different tile instead (the order of
+  // tiles does not change the result beyond fp32 rounding).
+  const int rot = DUSTIN_ATTN_ROTATE ? (int)(((long long)g * ntiles) / a.hkv) : 0;
+  auto tile_of = [&](int t) { int u = t + rot; return u >= ntiles ? u - ntiles : u; };
   const long long row_base =
       ((long long)bb * a.hq + (long long)g * a.group) * a.w;  // first q row
   const int r_lo = rb * C::ROWS;
@@ -202,6 +232,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(C::PRODUCER_REGS));
     const int pw = warp - C::NCW;
     const int my_row = pw * C::RPW + (lane % C::RPW);
+    static_assert(C::RPW <= 32, "one offset per lane");
     constexpr int LPR = 2 * C::CPR;   // lanes per row: K chunks, then V chunks
     constexpr int RPI = 32 / LPR;     // rows per warp instruction
     const int sub = lane / LPR;
@@ -211,8 +242,9 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
     const __nv_bfloat16* src_base = is_v ? a.kv.v : a.kv.k;
     unsigned char* dst_base = is_v ? sV : sK;
 
-    auto row_offset = [&](int t) -> long long {  // -1: leave the row out
-      const int i = t * C::TILE + my_row;
+    // Element offset of tile row r (-1: leave the row out).
+    auto row_offset = [&](int t, int r) -> long long {
+      const int i = t * C::TILE + r;
       if (i >= len) return -1;
       if constexpr (!DENSE) {
         return tab[i];
@@ -232,21 +264,33 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
         if (lane == 0) atomicOr(&g_attn_dev_flags, 4u);
         break;
       }
-      const long long my_off = row_offset(t);
+      const long long my_off = row_offset(tile_of(t), my_row);
       const unsigned vm = __ballot_sync(0xffffffffu, my_off >= 0) &
                           (C::RPW == 32 ? 0xffffffffu : ((1u << C::RPW) - 1u));
       unsigned char* dst = dst_base + s * C::TILE_BYTES + ch * 16;
 #pragma unroll 4
       for (int it = 0; it < C::RPW / RPI; ++it) {
-        const int rr = it * RPI + sub;
+        const int rr = it * RPI + sub;            // row within this warp's rows
         const long long off = __shfl_sync(0xffffffffu, my_off, rr);
+        const uint32_t d = smem_u32(dst + (pw * C::RPW + rr) * C::RS);
+#if DUSTIN_ATTN_PLAIN_CP
+        if (off >= 0)
+          cp_async_16_full(d, src_base + off + ch * 8);
+        else
+          cp_async_16(d, src_base, 0);            // zero-fill a left-out row
+#else
         const bool ok = off >= 0;
-        cp_async_16(smem_u32(dst + (pw * C::RPW + rr) * C::RS),
-                    src_base + (ok ? off + ch * 8 : 0), ok ? 16 : 0);
+        cp_async_16(d, src_base + (ok ? off + ch * 8 : 0), ok ? 16 : 0);
+#endif
       }
       cp_async_mbar_arrive(full_bar(s));
       if (lane == 0) {
-        sMask[s * C::NPW + pw] = vm;
+        if constexpr (C::RPW == 16)
+          reinterpret_cast<unsigned short*>(sMask64 + s)[pw] = (unsigned short)vm;
+        else if constexpr (C::RPW == 8)
+          reinterpret_cast<unsigned char*>(sMask64 + s)[pw] = (unsigned char)vm;
+        else
+          reinterpret_cast<unsigned*>(sMask64 + s)[pw] = vm;
         mbar_arrive(full_bar(s));
       }
     }
@@ -285,10 +329,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
     }
     const unsigned char* tk = sK + s * C::TILE_BYTES;
     const unsigned char* tv = sV + s * C::TILE_BYTES;
-    unsigned long long vmask = 0;
-#pragma unroll
-    for (int p = 0; p < C::NPW; ++p)
-      vmask |= (unsigned long long)sMask[s * C::NPW + p] << (p * C::RPW);
+    const unsigned long long vmask = sMask64[s];
 
     // S = Q K^T over this warp's PW positions.
     float sc[C::NT8][4];
@@ -296,6 +337,13 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
     for (int j = 0; j < C::NT8; ++j)
 #pragma unroll
       for (int e = 0; e < 4; ++e) sc[j][e] = 0.f;
+#if DUSTIN_ATTN_SPLIT_QK
+    float sc2[C::NT8][4];
+#pragma unroll
+    for (int j = 0; j < C::NT8; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sc2[j][e] = 0.f;
+#endif
 #pragma unroll
     for (int ks = 0; ks < C::KS; ++ks) {
 #pragma unroll
@@ -304,29 +352,39 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
         const int ch = ks * 2 + ((lane >> 3) & 1);
         uint32_t b0, b1, b2, b3;
         ldmatrix_x4(smem_u32(tk + r * C::RS + ch * 16), b0, b1, b2, b3);
+#if DUSTIN_ATTN_SPLIT_QK
+        if (ks & 1) {
+          mma_bf16(sc2[j], qf[ks], b0, b1);
+          mma_bf16(sc2[j + 1], qf[ks], b2, b3);
+          continue;
+        }
+#endif
         mma_bf16(sc[j], qf[ks], b0, b1);
         mma_bf16(sc[j + 1], qf[ks], b2, b3);
       }
     }
+#if DUSTIN_ATTN_SPLIT_QK
+#pragma unroll
+    for (int j = 0; j < C::NT8; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sc[j][e] += sc2[j][e];
+#endif
 
-    // Scale into log2 units; rows left out of the tile get -inf.
-    float mx0 = -INFINITY, mx1 = -INFINITY;
-    if (vmask == ~0ull) {
-#pragma unroll
-      for (int j = 0; j < C::NT8; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sc[j][e] *= a.scale_log2;
-    } else {
+    // Rows left out of the tile get -inf.  Scores stay unscaled here: the
+    // scale (> 0) is folded into the exponent below, so the maximum is taken
+    // on raw scores and converted once per row.
+    if (vmask != ~0ull) {
 #pragma unroll
       for (int j = 0; j < C::NT8; ++j)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int pos = wn * C::PW + j * 8 + 2 * tq + e;
           const bool ok = (vmask >> pos) & 1ull;
-          sc[j][e] = ok ? sc[j][e] * a.scale_log2 : -INFINITY;
-          sc[j][e + 2] = ok ? sc[j][e + 2] * a.scale_log2 : -INFINITY;
+          sc[j][e] = ok ? sc[j][e] : -INFINITY;
+          sc[j][e + 2] = ok ? sc[j][e + 2] : -INFINITY;
         }
     }
+    float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
     for (int j = 0; j < C::NT8; ++j) {
       mx0 = fmaxf(mx0, fmaxf(sc[j][0], sc[j][1]));
@@ -336,6 +394,8 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    mx0 *= a.scale_log2;   // log2 units (-inf stays -inf)
+    mx1 *= a.scale_log2;
     // Lazy rescale: move a row's reference maximum only when the tile's
     // maximum exceeds it by more than 2^kLazyRescale.
     const bool up0 = mx0 > m0 + kLazyRescale, up1 = mx1 > m1 + kLazyRescale;
@@ -357,12 +417,13 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
     }
     const float u0 = (m0 == -INFINITY) ? 0.f : m0;
     const float u1 = (m1 == -INFINITY) ? 0.f : m1;
+    const float c = a.scale_log2;
 #pragma unroll
     for (int j = 0; j < C::NT8; ++j) {
-      sc[j][0] = ex2(sc[j][0] - u0);
-      sc[j][1] = ex2(sc[j][1] - u0);
-      sc[j][2] = ex2(sc[j][2] - u1);
-      sc[j][3] = ex2(sc[j][3] - u1);
+      sc[j][0] = ex2(fmaf(sc[j][0], c, -u0));
+      sc[j][1] = ex2(fmaf(sc[j][1], c, -u0));
+      sc[j][2] = ex2(fmaf(sc[j][2], c, -u1));
+      sc[j][3] = ex2(fmaf(sc[j][3], c, -u1));
       l0 += sc[j][0] + sc[j][1];
       l1 += sc[j][2] + sc[j][3];
     }

@@ -39,8 +39,8 @@ struct AttnHost {
         cudaError_t e = cudaFuncGetAttributes(&fa, verify_attn_kernel<D, MT, PAGED, DENSE>);
         if (e != cudaSuccess) return e;
         const long long have = (long long)fa.numRegs * C::NT;
-        const long long need = (long long)C::PRODUCER_REGS * 128 +
-                               (long long)C::CONSUMER_REGS * (C::NT - 128);
+        const long long need = (long long)C::PRODUCER_REGS * C::NPW * 32 +
+                               (long long)C::CONSUMER_REGS * C::NCW * 32;
         checked.store(have >= need ? 1 : -1);
       }
       if (checked.load() < 0) return cudaErrorInvalidConfiguration;

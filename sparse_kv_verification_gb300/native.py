@@ -58,12 +58,14 @@ def library_path() -> str:
     return _build.LIB
 
 
-def load(build_if_missing: bool = False) -> ctypes.CDLL:
-    """Loads libdustin.so; raises if it is missing (there is no fallback)."""
+def load(build_if_missing: bool = False, path: Optional[str] = None
+         ) -> ctypes.CDLL:
+    """Loads libdustin.so (or the library at `path`, which then replaces the
+    loaded one); raises if it is missing (there is no fallback)."""
     global _LIB
-    if _LIB is not None:
+    if _LIB is not None and path is None:
         return _LIB
-    path = library_path()
+    path = path or library_path()
     if not os.path.exists(path):
         if not build_if_missing:
             raise RuntimeError(

@@ -85,6 +85,8 @@ def test_attention_validation(lib):
     assert sparse(lib, kv=kv(stride_n=132))[0] == 5
     assert sparse(lib, kv=kv(base=FAKE + 4))[0] == 5
     assert sparse(lib, scale=float("nan"))[0] == 1
+    assert sparse(lib, scale=0.0)[0] == 1
+    assert sparse(lib, scale=-0.5)[0] == 1
     assert sparse(lib, kv=kv(page_table=FAKE, page_size=8, ppseq=32,
                              pages=64))[0] == 3
     assert sparse(lib, kv=kv(page_table=FAKE, page_size=16, ppseq=4,

@@ -4,13 +4,17 @@
 // (alpha mode) or draft top-m followed by target top-(rest) (m mode).
 //
 // One CTA of 1024 threads per sequence.  Scores become order-preserving
-// uint32 keys (NaN lowest, -0 folded onto +0).  A three-pass radix select
-// (11 + 11 + 10 bits, shared-memory histograms, a block scan to find the
-// bucket holding the r-th key from the top) fixes the threshold key T and
-// how many keys equal to T to take; a marking pass over positions in
-// ascending order takes every key > T and the lowest-position keys == T
-// into a shared-memory bitmap.  A final ordered compaction writes the kept
-// positions (protected or marked) in ascending order.
+// uint32 keys (NaN lowest, -0 folded onto +0), computed once into shared
+// memory when the row fits (n <= 49152), else recomputed from global memory
+// in every pass.  A three-pass radix select (11 + 11 + 10 bits, one shared
+// histogram; lanes of a warp that hit the same bucket are merged with
+// __match_any_sync so each distinct bucket costs one atomic, which matters
+// because scores concentrate in few buckets; a block scan finds the bucket
+// holding the r-th key from the top) fixes the threshold key T and how many
+// keys equal to T to take; a marking pass over positions in ascending order
+// takes every key > T and the lowest-position keys == T into a shared-memory
+// bitmap.  A final ordered compaction writes the kept positions (protected
+// or marked) in ascending order.
 #include "device_common.cuh"
 #include "internal.h"
 
@@ -94,10 +98,21 @@ __device__ void select_mark(int r, int n, KeyF key, EligF elig, uint32_t* bits,
     const int nb = pass == 2 ? 1024 : 2048;
     for (int i = tid; i < 2048; i += kThreads) sh.hist[i] = 0;
     __syncthreads();
-    for (int j = tid; j < n; j += kThreads) {
-      if (!elig(j)) continue;
-      const uint32_t kj = key(j);
-      if ((kj & mask) == prefix) atomicAdd(&sh.hist[(kj >> shift) & (nb - 1)], 1);
+    // n is padded to whole warps so that __match_any_sync sees full warps.
+    const int n_pad = (n + 31) & ~31;
+    for (int j = tid; j < n_pad; j += kThreads) {
+      bool hit = false;
+      uint32_t bin = 0;
+      if (j < n && elig(j)) {
+        const uint32_t kj = key(j);
+        hit = (kj & mask) == prefix;
+        bin = (kj >> shift) & (nb - 1);
+      }
+      const unsigned hits = __ballot_sync(0xffffffffu, hit);
+      if (hits == 0u) continue;
+      const unsigned same = __match_any_sync(0xffffffffu, hit ? bin : 0xffffffffu);
+      const int lane = threadIdx.x & 31;
+      if (hit && (__ffs(same) - 1) == lane) atomicAdd(&sh.hist[bin], __popc(same));
     }
     __syncthreads();
     // Thread u owns the bins nb-1-u*bpt-q (q < bpt), i.e. bins from the top.
@@ -141,9 +156,13 @@ __device__ void select_mark(int r, int n, KeyF key, EligF elig, uint32_t* bits,
   __syncthreads();
 }
 
+constexpr int kSmemKeysMaxN = 49152;
+
+template <bool SMEM_KEYS>
 __global__ void __launch_bounds__(kThreads) select_kernel(const SelectArgs a) {
   extern __shared__ uint32_t bits[];
   __shared__ Shared sh;
+  uint32_t* skeys = bits + ((a.n + 31) / 32);   // only with SMEM_KEYS
   const int tid = threadIdx.x;
   const int n = a.n, k = a.k;
   int32_t* out = a.idx + (long long)blockIdx.x * min(k, n);
@@ -193,19 +212,40 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectArgs a) {
         c = 0.f;
       return order_key(c);
     };
-    select_mark(budget, n, mix, not_forced, bits, sh);
+    if constexpr (SMEM_KEYS) {
+      for (int j = tid; j < n; j += kThreads) skeys[j] = mix(j);
+      __syncthreads();
+      auto cached = [&](int j) { return skeys[j]; };
+      select_mark(budget, n, cached, not_forced, bits, sh);
+    } else {
+      select_mark(budget, n, mix, not_forced, bits, sh);
+    }
   } else {
     const int m_eff = min(a.m, budget);
-    if (m_eff > 0) {
-      auto kd = [&](int j) { return order_key(sd[j]); };
-      select_mark(m_eff, n, kd, not_forced, bits, sh);
-    }
-    if (budget - m_eff > 0) {
-      auto kt = [&](int j) { return order_key(st[j]); };
-      auto free_pos = [&](int j) {
-        return !forced(j) && !((bits[j >> 5] >> (j & 31)) & 1u);
-      };
-      select_mark(budget - m_eff, n, kt, free_pos, bits, sh);
+    auto free_pos = [&](int j) {
+      return !forced(j) && !((bits[j >> 5] >> (j & 31)) & 1u);
+    };
+    if constexpr (SMEM_KEYS) {
+      auto cached = [&](int j) { return skeys[j]; };
+      if (m_eff > 0) {
+        for (int j = tid; j < n; j += kThreads) skeys[j] = order_key(sd[j]);
+        __syncthreads();
+        select_mark(m_eff, n, cached, not_forced, bits, sh);
+      }
+      if (budget - m_eff > 0) {
+        for (int j = tid; j < n; j += kThreads) skeys[j] = order_key(st[j]);
+        __syncthreads();
+        select_mark(budget - m_eff, n, cached, free_pos, bits, sh);
+      }
+    } else {
+      if (m_eff > 0) {
+        auto kd = [&](int j) { return order_key(sd[j]); };
+        select_mark(m_eff, n, kd, not_forced, bits, sh);
+      }
+      if (budget - m_eff > 0) {
+        auto kt = [&](int j) { return order_key(st[j]); };
+        select_mark(budget - m_eff, n, kt, free_pos, bits, sh);
+      }
     }
   }
 
@@ -226,11 +266,13 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectArgs a) {
 
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t st) {
   const int words = (a.n + 31) / 32;
-  const int smem = words * 4;
+  const bool cache = a.n <= kSmemKeysMaxN && a.k < a.n;
+  const int smem = words * 4 + (cache ? a.n * 4 : 0);
+  auto kern = cache ? select_kernel<true> : select_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(
-      select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  select_kernel<<<a.b, kThreads, smem, st>>>(a);
+  kern<<<a.b, kThreads, smem, st>>>(a);
   e = cudaGetLastError();
   if (e == cudaSuccess) note_launches(1);
   return e;

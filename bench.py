@@ -209,26 +209,25 @@ class Replica:
             self.ws_f) for l in range(self.L)]
 
     def step(self, ev=None):
-        """One pass of the hot path; ev (optional) records per-phase events:
-        ev[0..3] around score/select, ev[4 + 2l], ev[5 + 2l] around layer l."""
-        if ev is None:
-            self.score_t()
-            self.score_d()
-            self.select()
-            for a in self.attn:
-                a()
-            return
-        ev[0].record()
+        """One pass of the hot path; ev (optional) records events at the
+        phase boundaries only (score target | score draft | select | all
+        layers' attention), so consecutive kernels keep their programmatic
+        dependent launch."""
+        if ev is not None:
+            ev[0].record()
         self.score_t()
-        ev[1].record()
+        if ev is not None:
+            ev[1].record()
         self.score_d()
-        ev[2].record()
+        if ev is not None:
+            ev[2].record()
         self.select()
-        ev[3].record()
-        for l, a in enumerate(self.attn):
-            ev[4 + 2 * l].record()
+        if ev is not None:
+            ev[3].record()
+        for a in self.attn:
             a()
-            ev[5 + 2 * l].record()
+        if ev is not None:
+            ev[4].record()
 
     # Algorithmic bytes (what the method must move), per launch / per step.
     def bytes_sparse_launch(self):
@@ -405,7 +404,7 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
 
     # ---- timed region: K steps, per-phase events on the launch stream.
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4 + 2 * L)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)]
            for _ in range(K)]
     start, end = (torch.cuda.Event(enable_timing=True),
                   torch.cuda.Event(enable_timing=True))
@@ -431,9 +430,10 @@ def run_ours(args):
     t_score_t = avg(0, 1)
     t_score_d = avg(1, 2)
     t_select = avg(2, 3)
-    attn_us = [evs[i][4 + 2 * l].elapsed_time(evs[i][5 + 2 * l]) * 1e3
-               for i in range(K) for l in range(L)]
-    t_attn = statistics.mean(attn_us)
+    # Average launch duration of the sparse attention: the attention phase
+    # of each step divided by its launches (back-to-back launches; the gaps
+    # between them are included, so this is conservative).
+    t_attn = avg(3, 4) / L
 
     tokens = wl.b * wl.w * L
     value = R.reduce_sum(tokens, dev) / (t_ms * 1e-3)
@@ -447,17 +447,16 @@ def run_ours(args):
         for full in rep.full[:2]:
             full()
         torch.cuda.synchronize(dev)
-        ds = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * L)]
+        ds = [(torch.cuda.Event(enable_timing=True),
+               torch.cuda.Event(enable_timing=True))
               for _ in range(args.dense_steps)]
         for i in range(args.dense_steps):
-            for l, full in enumerate(rep.full):
-                ds[i][2 * l].record()
+            ds[i][0].record()
+            for full in rep.full:
                 full()
-                ds[i][2 * l + 1].record()
+            ds[i][1].record()
         torch.cuda.synchronize(dev)
-        per = [ds[i][2 * l].elapsed_time(ds[i][2 * l + 1]) * 1e3
-               for i in range(args.dense_steps) for l in range(L)]
-        t_dense = statistics.mean(per)
+        t_dense = statistics.mean(a.elapsed_time(b) * 1e3 / L for a, b in ds)
         b_dense = rep.bytes_dense_launch()
         dense = {"us_per_layer": t_dense,
                  "hbm_gbs": b_dense / (t_dense * 1e-6) / 1e9,

@@ -168,6 +168,9 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
       ((long long)bb * a.hq + (long long)g * a.group) * a.w;  // first q row
   const int r_lo = rb * C::ROWS;
 
+  griddep_wait();
+  griddep_launch_dependents();
+
   // ---- Q rows into shared memory (zero rows past G*w), barriers.
   for (int c = tid; c < C::ROWS * C::CPR; c += C::NT) {
     const int r = c / C::CPR, ch = c % C::CPR;
@@ -547,6 +550,8 @@ __global__ void __launch_bounds__(256)
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int nblk = a.b * a.hkv * a.row_blocks;
+  griddep_wait();
+  griddep_launch_dependents();
   if (warp >= nblk * C::ROWS) return;
   const int r = warp % C::ROWS;
   const int blk = warp / C::ROWS;

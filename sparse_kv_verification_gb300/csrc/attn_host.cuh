@@ -54,15 +54,14 @@ struct AttnHost {
     cudaError_t e = prepare<D, MT, PAGED>();
     if (e != cudaSuccess) return e;
     const long long blocks = (long long)a.b * a.hkv * a.row_blocks;
-    verify_attn_kernel<D, MT, PAGED, DENSE>
-        <<<(unsigned)(blocks * a.splits), C::NT, C::SMEM, st>>>(a);
-    e = cudaGetLastError();
+    e = launch_pdl(verify_attn_kernel<D, MT, PAGED, DENSE>,
+                   dim3((unsigned)(blocks * a.splits)), dim3(C::NT), C::SMEM, st, a);
     if (e != cudaSuccess) return e;
     note_launches(1);
     if (a.splits > 1) {
       const long long warps = blocks * C::ROWS;
-      attn_combine_kernel<D, MT><<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(a);
-      e = cudaGetLastError();
+      e = launch_pdl(attn_combine_kernel<D, MT>, dim3((unsigned)((warps + 7) / 8)),
+                     dim3(256), 0, st, a);
       if (e != cudaSuccess) return e;
       note_launches(1);
     }

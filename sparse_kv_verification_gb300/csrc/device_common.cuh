@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <utility>
 
 namespace dustin {
 
@@ -155,6 +156,20 @@ __device__ __forceinline__ void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(threads) : "memory");
 }
 
+// Programmatic dependent launch.  Every kernel of this library is launched
+// with programmatic stream serialisation, so it may start while the
+// previous kernel on the stream drains: it waits (griddepcontrol.wait)
+// before its first global-memory access, which orders it after that
+// kernel's completion, and lets the next kernel launch early once its own
+// main work is issued (griddepcontrol.launch_dependents).  Both are no-ops
+// without a programmatic dependency.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 // About one second at GB300 clocks: the limit of every mbarrier wait.
 constexpr long long kWaitLimitCycles = 2000000000LL;
 
@@ -162,3 +177,24 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 }  // namespace dustin
+
+#ifndef __CUDACC_RTC__
+namespace dustin {
+// Launches `kern` with programmatic stream serialisation allowed.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block,
+                       size_t smem, cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+}  // namespace dustin
+#endif

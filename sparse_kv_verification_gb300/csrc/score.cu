@@ -65,6 +65,8 @@ __global__ void __launch_bounds__(kThreads)
   const int len = max(0, p_end - p_begin);
   const int ntiles = (len + kTile - 1) / kTile;
   const long long unit_off = (long long)bb * kv.sb + (long long)pr.kv_head * kv.sh;
+  griddep_wait();
+  griddep_launch_dependents();
 
   // Query rows of this (pair, sequence): q[p][b][r][D], zero past `rows`.
   const __nv_bfloat16* qb = a.q + ((long long)p * a.b + bb) * a.rows * D;
@@ -211,6 +213,8 @@ __global__ void __launch_bounds__(256) score_reduce_kernel(const ScoreArgs a) {
   __shared__ float lse2[1024];
   const int bb = blockIdx.y;
   const int prs = a.n_pairs * a.rows;
+  griddep_wait();
+  griddep_launch_dependents();
   for (int i = threadIdx.x; i < prs; i += blockDim.x) {
     const float2* st = a.stats + ((long long)i * a.b + bb) * a.nchunks;
     float M = -INFINITY;
@@ -242,13 +246,11 @@ cudaError_t run_score(const ScoreArgs& a, cudaStream_t st) {
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const long long grid = (long long)a.n_pairs * a.b * a.nchunks;
-  kern<<<(unsigned)grid, kThreads, C::SMEM, st>>>(a);
-  e = cudaGetLastError();
+  e = launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), C::SMEM, st, a);
   if (e != cudaSuccess) return e;
   note_launches(1);
   dim3 g2((unsigned)((a.n + 1023) / 1024), (unsigned)a.b);
-  score_reduce_kernel<<<g2, 256, 0, st>>>(a);
-  e = cudaGetLastError();
+  e = launch_pdl(score_reduce_kernel, g2, dim3(256), 0, st, a);
   if (e == cudaSuccess) note_launches(1);
   return e;
 }

@@ -168,6 +168,8 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectArgs a) {
   int32_t* out = a.idx + (long long)blockIdx.x * min(k, n);
   const float* sd = a.sd ? a.sd + (long long)blockIdx.x * n : nullptr;
   const float* st = a.st ? a.st + (long long)blockIdx.x * n : nullptr;
+  griddep_wait();
+  griddep_launch_dependents();
   if (k >= n) {
     for (int j = tid; j < n; j += kThreads) out[j] = j;
     return;
@@ -272,8 +274,7 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<a.b, kThreads, smem, st>>>(a);
-  e = cudaGetLastError();
+  e = launch_pdl(kern, dim3(a.b), dim3(kThreads), smem, st, a);
   if (e == cudaSuccess) note_launches(1);
   return e;
 }

@@ -181,8 +181,14 @@ class Replica:
         self.s_d = torch.empty((b, n), device=device)
         self.idx = torch.empty((b, min(wl.k, n)), dtype=torch.int32,
                                device=device)
-        self.o = [torch.empty_like(q) for q in inp.q]
-        self.lse = [torch.empty(q.shape[:3], device=device) for q in inp.q]
+        # All layers' queries and outputs live in one contiguous buffer each,
+        # so the end-to-end leg moves them with one copy per direction.
+        self.q_all = torch.stack(inp.q)
+        inp.q = [self.q_all[l] for l in range(self.L)]
+        self.o_all = torch.empty_like(self.q_all)
+        self.lse_all = torch.empty(self.q_all.shape[:4], device=device)
+        self.o = [self.o_all[l] for l in range(self.L)]
+        self.lse = [self.lse_all[l] for l in range(self.L)]
         self.ws_t = N.workspace(N.dustin_score_heads_workspace_size(
             b, n, wl.p_t, 1), device)
         self.ws_d = N.workspace(N.dustin_score_heads_workspace_size(
@@ -469,9 +475,9 @@ def run_ours(args):
     e2e = None
     if not args.no_e2e:
         inp = rep.inp
-        h_in = [t.cpu().pin_memory() for t in ([inp.q_t, inp.q_d] + inp.q)]
-        d_in = [inp.q_t, inp.q_d] + inp.q
-        d_out = rep.o + rep.lse + [rep.idx]
+        d_in = [inp.q_t, inp.q_d, rep.q_all]
+        h_in = [t.cpu().pin_memory() for t in d_in]
+        d_out = [rep.o_all, rep.lse_all, rep.idx]
         h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
                  for t in d_out]
         h2d = sum(t.numel() * t.element_size() for t in h_in)

@@ -2,12 +2,14 @@
 // include/dustin.h): host-side validation, launch planning and dispatch.
 // Nothing here allocates device memory; scratch comes from the caller.
 #include <atomic>
+#include <chrono>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
 
 #include "attn.cuh"
+#include "attn_streamk.cuh"
 #include "dustin.h"
 #include "internal.h"
 
@@ -109,42 +111,95 @@ int check_kv(const dustin_kv* kv, int b, int n, int d, bool need_v,
 }
 
 // ---- attention planning
+// Shared by both kernels: a unit is (sequence, kv head, row block of at
+// most 64 query rows, in 16-row tiles).
 struct AttnPlan {
-  int mt, row_blocks, splits, chunk;
-  size_t ws_o, ws_ml;
+  int mt, row_blocks, tpu;
+  long long units;
+  // sparse: positions split `splits` ways, `chunk` positions each.
+  int splits, chunk;
+  // dense: stream-K over `grid` CTAs; `split` when some unit is shared.
+  long long grid;
+  bool split;
+  size_t ws_o, ws_ml, ws_cnt;
+  size_t workspace() const { return ws_o + ws_ml + ws_cnt; }
 };
 
-AttnPlan plan_attn(bool dense, int b, int hq, int hkv, int d, int w, int npos) {
-  AttnPlan p;
-  const int group = hq / hkv;
-  const long long rows = (long long)group * w;
-  p.mt = (int)std::min<long long>(4, (rows + 15) / 16);
-  if (p.mt < 1) p.mt = 1;
+AttnPlan plan_units(int hq, int hkv, int w, int b, int npos) {
+  AttnPlan p{};
+  const long long rows = (long long)(hq / hkv) * w;
+  p.mt = (int)std::min<long long>(4, std::max<long long>(1, (rows + 15) / 16));
   p.row_blocks = (int)((rows + 16 * p.mt - 1) / (16 * p.mt));
-  const long long units = (long long)b * hkv * p.row_blocks;
-  const int tiles = (npos + 63) / 64;
-  if (tiles == 0 || units == 0) {
-    p.splits = 1;
-    p.chunk = 64;
-  } else {
-    const long long slots = (long long)attn_slots(dense, d, p.mt);
-    long long s = units >= slots ? 1 : slots / units;
+  p.units = (long long)b * hkv * p.row_blocks;
+  p.tpu = std::max(1, (npos + 63) / 64);
+  return p;
+}
+
+// Sparse: one CTA per unit; when the units leave SMs idle, the positions
+// of each unit are split into equal ranges (at most 2048 rows each, the
+// kernel's offset table) and merged by a combine kernel.
+AttnPlan plan_sparse(int b, int hq, int hkv, int d, int w, int k) {
+  AttnPlan p = plan_units(hq, hkv, w, b, k);
+  const int tiles = (k + 63) / 64;
+  p.splits = 1;
+  p.chunk = 64;
+  if (tiles > 0 && p.units > 0) {
+    const long long slots = (long long)attn_slots(false, d, p.mt);
+    long long s = p.units >= slots ? 1 : slots / p.units;
     s = std::min<long long>(s, tiles);
-    long long ct = (tiles + s - 1) / s;
-    // Offset-table cap: 2048 rows (sparse) or 2047 pages of >= 16 (dense).
-    const long long cap = dense ? (2047LL * 16) / 64 : 2048 / 64;
-    ct = std::min(ct, cap);
+    long long ct = std::min<long long>((tiles + s - 1) / s, 2048 / 64);
     p.splits = (int)((tiles + ct - 1) / ct);
     p.chunk = (int)(ct * 64);
   }
   if (p.splits > 1) {
-    const size_t prows = (size_t)units * p.splits * 16 * p.mt;
+    const size_t prows = (size_t)p.units * p.splits * 16 * p.mt;
     p.ws_o = align256(prows * d * sizeof(float));
     p.ws_ml = align256(prows * sizeof(float2));
-  } else {
-    p.ws_o = p.ws_ml = 0;
   }
   return p;
+}
+
+// Build-time tunable: an upper bound on the CTAs one dense launch keeps
+// resident (0: all that fit).
+#ifndef DUSTIN_ATTN_GRID_CAP
+#define DUSTIN_ATTN_GRID_CAP 0
+#endif
+
+// Dense: stream-K over tiles.  G is the number of CTAs resident at once,
+// raised where a CTA's range would overflow its page table (512 tiles).
+AttnPlan plan_dense(int b, int hq, int hkv, int d, int w, int n) {
+  AttnPlan p = plan_units(hq, hkv, w, b, n);
+  const long long T = p.units * p.tpu;
+  if (T <= 0) return p;
+  long long slots = (long long)attn_slots(true, d, p.mt);
+#if DUSTIN_ATTN_GRID_CAP > 0
+  slots = std::min<long long>(slots, DUSTIN_ATTN_GRID_CAP);
+#endif
+  const long long cap = 2048 / 4;
+  p.grid = std::max(std::min(slots, T), (T + cap - 1) / cap);
+  // Every range boundary c T / G falls on a unit boundary when G divides
+  // the unit count (conservatively "split" otherwise).
+  p.split = p.tpu > 1 && p.units % p.grid != 0;
+  if (p.split) {
+    const size_t prows = (size_t)(2 * p.grid) * 16 * p.mt;
+    p.ws_o = align256(prows * d * sizeof(float));
+    p.ws_ml = align256(prows * sizeof(float2));
+    p.ws_cnt = align256((size_t)p.units * sizeof(unsigned long long));
+  }
+  return p;
+}
+
+// A fresh nonzero 40-bit tag per dense call, so counter words left by
+// earlier calls (or never written) read as zero.
+unsigned long long next_epoch() {
+  static std::atomic<unsigned long long> ctr{
+      (unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count()};
+  constexpr unsigned long long kMask = (1ull << 40) - 1;
+  unsigned long long e;
+  do {
+    e = ctr.fetch_add(1) & kMask;
+  } while (e == 0);
+  return e;
 }
 
 int check_attn_shape(int b, int hq, int hkv, int d, int w, int n,
@@ -187,38 +242,76 @@ int run_attn(bool dense, int b, int hq, int hkv, int d, int w, int n, int k,
     return fail(DUSTIN_ERR_INVALID_ARG, "%s: scale must be finite and > 0", what);
   rc = check_kv(kv, b, n, d, true, what);
   if (rc) return rc;
-  const int npos = dense ? n : k;
-  AttnPlan p = plan_attn(dense, b, hq, hkv, d, w, npos);
-  if ((long long)b * hkv * p.row_blocks * p.splits > 0x7fffffffLL)
-    return fail(DUSTIN_ERR_SHAPE, "%s: grid too large", what);
-  const size_t need = p.ws_o + p.ws_ml;
-  if (need > 0 && (!ws || ws_bytes < need || !aligned16(ws)))
-    return fail(DUSTIN_ERR_WORKSPACE, "%s: workspace %zu bytes, need %zu (16-byte aligned)",
-                what, ws_bytes, need);
-  AttnArgs a;
-  a.q = static_cast<const __nv_bfloat16*>(q);
-  a.o = static_cast<__nv_bfloat16*>(o);
-  a.lse = lse;
-  a.kv = to_view(*kv);
-  a.idx = dense ? nullptr : idx;
-  a.b = b;
-  a.hq = hq;
-  a.hkv = hkv;
-  a.w = w;
-  a.n = n;
-  a.npos = npos;
-  a.group = hq / hkv;
-  a.rows = a.group * w;
-  a.row_blocks = p.row_blocks;
-  a.splits = p.splits;
-  a.chunk = p.chunk;
-  a.scale_log2 = scale * kLog2e;
-  a.ws_o = need ? static_cast<float*>(ws) : nullptr;
-  a.ws_ml = need ? reinterpret_cast<float2*>(static_cast<char*>(ws) + p.ws_o)
-                 : nullptr;
   const bool paged = kv->page_table != nullptr;
-  cudaError_t e = dense ? launch_attn_dense(a, d, p.mt, paged, (cudaStream_t)stream)
-                        : launch_attn_sparse(a, d, p.mt, paged, (cudaStream_t)stream);
+  cudaError_t e;
+  if (!dense) {
+    const AttnPlan p = plan_sparse(b, hq, hkv, d, w, k);
+    if (p.units * p.splits > 0x7fffffffLL)
+      return fail(DUSTIN_ERR_SHAPE, "%s: grid too large", what);
+    const size_t need = p.workspace();
+    if (need > 0 && (!ws || ws_bytes < need || !aligned16(ws)))
+      return fail(DUSTIN_ERR_WORKSPACE,
+                  "%s: workspace %zu bytes, need %zu (16-byte aligned)", what,
+                  ws_bytes, need);
+    AttnArgs a;
+    a.q = static_cast<const __nv_bfloat16*>(q);
+    a.o = static_cast<__nv_bfloat16*>(o);
+    a.lse = lse;
+    a.kv = to_view(*kv);
+    a.idx = idx;
+    a.b = b;
+    a.hq = hq;
+    a.hkv = hkv;
+    a.w = w;
+    a.n = n;
+    a.npos = k;
+    a.group = hq / hkv;
+    a.rows = a.group * w;
+    a.row_blocks = p.row_blocks;
+    a.splits = p.splits;
+    a.chunk = p.chunk;
+    a.scale_log2 = scale * kLog2e;
+    a.ws_o = need ? static_cast<float*>(ws) : nullptr;
+    a.ws_ml = need ? reinterpret_cast<float2*>(static_cast<char*>(ws) + p.ws_o)
+                   : nullptr;
+    e = launch_attn_sparse(a, d, p.mt, paged, (cudaStream_t)stream);
+  } else {
+    const AttnPlan p = plan_dense(b, hq, hkv, d, w, n);
+    const long long T = p.units * p.tpu;
+    if (p.units > 0x7fffffffLL || p.grid > 0x7fffffffLL || T > (1LL << 40) ||
+        p.grid * T > (1LL << 62) ||
+        p.tpu / std::max(1LL, T / std::max(1LL, p.grid)) + 2 > (1LL << 24) - 1)
+      return fail(DUSTIN_ERR_SHAPE, "%s: problem too large", what);
+    const size_t need = p.workspace();
+    if (need > 0 && (!ws || ws_bytes < need || !aligned16(ws)))
+      return fail(DUSTIN_ERR_WORKSPACE,
+                  "%s: workspace %zu bytes, need %zu (16-byte aligned)", what,
+                  ws_bytes, need);
+    AttnSkArgs a;
+    a.q = static_cast<const __nv_bfloat16*>(q);
+    a.o = static_cast<__nv_bfloat16*>(o);
+    a.lse = lse;
+    a.kv = to_view(*kv);
+    a.b = b;
+    a.hq = hq;
+    a.hkv = hkv;
+    a.w = w;
+    a.n = n;
+    a.group = hq / hkv;
+    a.rows = a.group * w;
+    a.row_blocks = p.row_blocks;
+    a.units = (int)p.units;
+    a.tpu = p.tpu;
+    a.grid = (int)p.grid;
+    a.scale_log2 = scale * kLog2e;
+    char* wsb = static_cast<char*>(ws);
+    a.ws_o = need ? reinterpret_cast<float*>(wsb) : nullptr;
+    a.ws_ml = need ? reinterpret_cast<float2*>(wsb + p.ws_o) : nullptr;
+    a.counters = need ? reinterpret_cast<unsigned long long*>(wsb + p.ws_o + p.ws_ml)
+                      : nullptr;
+    a.epoch = next_epoch();
+    e = launch_attn_dense(a, d, p.mt, paged, (cudaStream_t)stream);
+  }
   if (e != cudaSuccess) return cuda_fail(e, what);
   return DUSTIN_OK;
 }
@@ -395,8 +488,7 @@ size_t dustin_sparse_verify_attn_workspace_size(int b, int h_q, int h_kv, int d,
   if (b <= 0 || h_q <= 0 || h_kv <= 0 || h_q % h_kv || w <= 0 || k < 0 ||
       (d != 64 && d != 128))
     return 0;
-  AttnPlan p = plan_attn(false, b, h_q, h_kv, d, w, k);
-  return p.ws_o + p.ws_ml;
+  return plan_sparse(b, h_q, h_kv, d, w, k).workspace();
 }
 
 int dustin_sparse_verify_attn(int b, int h_q, int h_kv, int d, int w, int n,
@@ -413,8 +505,7 @@ size_t dustin_full_verify_attn_workspace_size(int b, int h_q, int h_kv, int d,
   if (b <= 0 || h_q <= 0 || h_kv <= 0 || h_q % h_kv || w <= 0 || n < 0 ||
       (d != 64 && d != 128))
     return 0;
-  AttnPlan p = plan_attn(true, b, h_q, h_kv, d, w, n);
-  return p.ws_o + p.ws_ml;
+  return plan_dense(b, h_q, h_kv, d, w, n).workspace();
 }
 
 int dustin_full_verify_attn(int b, int h_q, int h_kv, int d, int w, int n,

@@ -1,30 +1,35 @@
-// Verification attention for Dustin's Stage 2 (sparse verification over the
-// selected KV; "dustin-long-context" notes section 2.2, Fig. 5) and the
-// full-cache baseline (notes section 3, Fig. 7).
+// Sparse verification attention, Dustin's Stage 2 (verification over the
+// selected KV; "dustin-long-context" notes section 2.2, Fig. 5): every query
+// row of the window against the k positions idx[b][0..k) of its sequence.
 //
 // One CTA handles one (sequence b, kv head g, row block, split): the G*w
 // query rows that share kv head g (query heads g*G .. g*G+G-1, w window
 // rows each: a contiguous [G*w][d] block of q) against a contiguous range
-// of the unit's positions.  Positions are idx[b][i] (sparse) or i (dense).
+// of the selected positions.  A sparse unit is short (32 tiles of 64 at
+// k = 2048), so one CTA per unit is the fastest schedule whenever the units
+// come near filling the GPU (128 on 152 SMs at the 72B shape): splitting a
+// unit across CTAs only adds a merge to a loop already near the gather
+// ceiling.  When they do not, the positions are split into `splits` equal
+// ranges and attn_combine_kernel merges the partials.
 //
 // Warp-specialised pipeline:
 //  * a producer warpgroup (4 warps) gathers each 64-position tile, 16 rows
 //    per warp: one warp instruction of 16-byte cp.async copies a whole K row
 //    and V row (d = 128; two rows for d = 64) into padded shared-memory rows
-//    (2*d + 16 bytes, so
-//    ldmatrix of eight rows is conflict-free).  Each producer thread then
-//    arms cp.async.mbarrier.arrive on the stage's "full" mbarrier, and lane 0
-//    publishes the warp's 32-row valid mask with a plain (release) arrive.
-//    Row offsets come from a shared-memory table that every thread of the CTA
-//    fills once from idx (and the page table) before the pipeline starts, so
-//    no global-load latency sits inside the producer loop.
-//    Rows that fail a check, and rows past the range, are zero-filled by the
-//    copy (source size 0) and left out through the valid mask.  (Measured on
-//    a 72B-shaped gather of 256-byte rows: 16-byte cp.async reaches 4.3, 5.0
-//    and 5.2 TB/s with 2, 4 and 8 producer warps, per-row TMA bulk copies
-//    1.1 TB/s and TMA tile::gather4 1.8 TB/s, so cp.async does the gather.)
-//    With 16 warps (three consumer warpgroups) the producers hand registers
-//    to the consumers with setmaxnreg (40 / 152 of a 128-register launch).
+//    (2*d + 16 bytes, so ldmatrix of eight rows is conflict-free).  Each
+//    producer thread then arms cp.async.mbarrier.arrive on the stage's
+//    "full" mbarrier, and lane 0 publishes the warp's valid-row mask with a
+//    plain (release) arrive.  Row offsets come from a shared-memory table
+//    that every thread of the CTA fills once from idx (and the page table)
+//    before the pipeline starts, so no global-load latency sits inside the
+//    producer loop.  Rows that fail a check, and rows past the range, are
+//    zero-filled by the copy (source size 0) and left out through the valid
+//    mask.  (Measured on a 72B-shaped gather of 256-byte rows: 16-byte
+//    cp.async reaches 4.3, 5.0 and 5.2 TB/s with 2, 4 and 8 producer warps,
+//    per-row TMA bulk copies 1.1 TB/s and TMA tile::gather4 1.8 TB/s, so
+//    cp.async does the gather.)  With 16 warps (three consumer warpgroups)
+//    the producers hand registers to the consumers with setmaxnreg (40 / 152
+//    of a 128-register launch).
 //  * MT*WN consumer warps: warp (wm, wn) owns query rows [16 wm, 16 wm + 16)
 //    and a 64/WN-position slice of every tile.  S = Q K^T and O += P V run on
 //    bf16 mma.sync m16n8k16 with fp32 accumulators; the softmax is online in
@@ -48,9 +53,9 @@ struct AttnArgs {
   __nv_bfloat16* o;
   float* lse;
   KvView kv;
-  const int* idx;   // [b][npos] (sparse) or nullptr (dense)
+  const int* idx;   // [b][npos]
   int b, hq, hkv, w, n;
-  int npos;         // positions per (b, kv head): k or n
+  int npos;         // selected positions per sequence: k
   int group;        // hq / hkv
   int rows;         // group * w
   int row_blocks;   // ceil(rows / (16 * MT))
@@ -122,9 +127,8 @@ struct AttnCfg {
 // Device-side check flags of this translation unit.
 static __device__ unsigned int g_attn_dev_flags;
 
-constexpr float kLazyRescale = 8.0f;  // log2 units
 
-template <int D, int MT, bool PAGED, bool DENSE>
+template <int D, int MT, bool PAGED>
 __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
     verify_attn_kernel(const AttnArgs a) {
   using C = AttnCfg<D, MT>;
@@ -187,9 +191,9 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
     }
     mbar_fence_init();
   }
-  // Offset table: element offset of each position's K/V row (sparse), or of
-  // each page (dense, paged); -1 marks a row that failed a check.
-  if constexpr (!DENSE) {
+  // Offset table: element offset of each position's K/V row; -1 marks a
+  // row that failed a check.
+  {
     const int* idx_row = a.idx + (long long)bb * a.npos + p_begin;
     for (int i = tid; i < len; i += C::NT) {
       const int j = __ldg(idx_row + i);
@@ -207,19 +211,6 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
       } else {
         off = unit_off + (long long)j * a.kv.sn;
       }
-      tab[i] = off;
-    }
-  } else if constexpr (PAGED) {
-    const int pg0 = p_begin / a.kv.page_size;
-    const int npg = len > 0 ? (p_end - 1) / a.kv.page_size - pg0 + 1 : 0;
-    for (int i = tid; i < npg; i += C::NT) {
-      const int pg = __ldg(a.kv.page_table + (long long)bb * a.kv.pages_per_seq +
-                           pg0 + i);
-      long long off = -1;
-      if (pg < 0 || pg >= a.kv.num_pages)
-        atomicOr(&g_attn_dev_flags, 2u);
-      else
-        off = (long long)pg * a.kv.sb + (long long)g * a.kv.sh;
       tab[i] = off;
     }
   }
@@ -248,16 +239,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
     // Element offset of tile row r (-1: leave the row out).
     auto row_offset = [&](int t, int r) -> long long {
       const int i = t * C::TILE + r;
-      if (i >= len) return -1;
-      if constexpr (!DENSE) {
-        return tab[i];
-      } else if constexpr (PAGED) {
-        const int j = p_begin + i;
-        const long long base = tab[j / a.kv.page_size - p_begin / a.kv.page_size];
-        return base < 0 ? -1 : base + (long long)(j % a.kv.page_size) * a.kv.sn;
-      } else {
-        return unit_off + (long long)(p_begin + i) * a.kv.sn;
-      }
+      return i < len ? tab[i] : -1;
     };
 
     for (int t = 0; t < ntiles; ++t) {

@@ -1,5 +1,5 @@
-// Host-side launch of the verification-attention kernels (one instance set
-// per translation unit: sparse or dense).
+// Host-side launch of the sparse verification-attention kernel and its
+// split combine (attn.cuh).
 #pragma once
 
 #include <atomic>
@@ -9,21 +9,6 @@
 
 namespace dustin {
 
-// Sets the dynamic shared-memory limit of `kern` once per device.
-template <typename K>
-cudaError_t ensure_smem_attr(K kern, int bytes, std::atomic<uint64_t>& done) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  const uint64_t bit = 1ull << (dev & 63);
-  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           bytes);
-  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
-  return e;
-}
-
-template <bool DENSE>
 struct AttnHost {
   template <int D, int MT, bool PAGED>
   static cudaError_t prepare() {
@@ -36,7 +21,7 @@ struct AttnHost {
       static std::atomic<int> checked{0};
       if (checked.load() == 0) {
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, verify_attn_kernel<D, MT, PAGED, DENSE>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, verify_attn_kernel<D, MT, PAGED>);
         if (e != cudaSuccess) return e;
         const long long have = (long long)fa.numRegs * C::NT;
         const long long need = (long long)C::PRODUCER_REGS * C::NPW * 32 +
@@ -45,7 +30,7 @@ struct AttnHost {
       }
       if (checked.load() < 0) return cudaErrorInvalidConfiguration;
     }
-    return ensure_smem_attr(verify_attn_kernel<D, MT, PAGED, DENSE>, C::SMEM, done);
+    return ensure_smem_attr(verify_attn_kernel<D, MT, PAGED>, C::SMEM, done);
   }
 
   template <int D, int MT, bool PAGED>
@@ -54,7 +39,7 @@ struct AttnHost {
     cudaError_t e = prepare<D, MT, PAGED>();
     if (e != cudaSuccess) return e;
     const long long blocks = (long long)a.b * a.hkv * a.row_blocks;
-    e = launch_pdl(verify_attn_kernel<D, MT, PAGED, DENSE>,
+    e = launch_pdl(verify_attn_kernel<D, MT, PAGED>,
                    dim3((unsigned)(blocks * a.splits)), dim3(C::NT), C::SMEM, st, a);
     if (e != cudaSuccess) return e;
     note_launches(1);
@@ -89,7 +74,7 @@ struct AttnHost {
     if (prepare<D, MT, false>() != cudaSuccess) return 1;
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &n, verify_attn_kernel<D, MT, false, DENSE>, AttnCfg<D, MT>::NT,
+            &n, verify_attn_kernel<D, MT, false>, AttnCfg<D, MT>::NT,
             AttnCfg<D, MT>::SMEM) != cudaSuccess)
       return 1;
     return n > 0 ? n : 1;

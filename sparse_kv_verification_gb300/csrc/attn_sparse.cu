@@ -6,15 +6,13 @@ namespace dustin {
 
 cudaError_t launch_attn_sparse(const AttnArgs& a, int d, int mt, bool paged,
                                cudaStream_t st) {
-  return AttnHost<false>::launch(a, d, mt, paged, st);
+  return AttnHost::launch(a, d, mt, paged, st);
 }
 
-int occupancy_attn_sparse(int d, int mt) {
-  return AttnHost<false>::occupancy(d, mt);
-}
+int occupancy_attn_sparse(int d, int mt) { return AttnHost::occupancy(d, mt); }
 
 cudaError_t take_attn_sparse_flags(unsigned* flags) {
-  return AttnHost<false>::take_flags(flags);
+  return AttnHost::take_flags(flags);
 }
 
 }  // namespace dustin

@@ -3,6 +3,8 @@
 // the exp2 instruction and an XOR swizzle for [rows][d] bf16 tiles.
 #pragma once
 
+#include <atomic>
+
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -175,12 +177,29 @@ constexpr long long kWaitLimitCycles = 2000000000LL;
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+// Lazy softmax rescale threshold of the attention kernels (log2 units): a
+// row's reference maximum moves only when a tile's maximum exceeds it by more.
+constexpr float kLazyRescale = 8.0f;
 
 }  // namespace dustin
 
 #ifndef __CUDACC_RTC__
 namespace dustin {
 // Launches `kern` with programmatic stream serialisation allowed.
+// Sets the dynamic shared-memory limit of `kern` once per device.
+template <typename K>
+cudaError_t ensure_smem_attr(K kern, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           bytes);
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block,
                        size_t smem, cudaStream_t st, Args&&... args) {

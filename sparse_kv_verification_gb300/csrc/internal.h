@@ -44,11 +44,13 @@ struct SelectArgs {
 constexpr int kSelectMaxN = 1 << 20;
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t st);
 
-// ---- verification attention (declared in attn.cuh: AttnArgs)
+// ---- verification attention (AttnArgs in attn.cuh, AttnSkArgs in
+// attn_streamk.cuh)
 struct AttnArgs;
+struct AttnSkArgs;
 cudaError_t launch_attn_sparse(const AttnArgs& a, int d, int mt, bool paged,
                                cudaStream_t st);
-cudaError_t launch_attn_dense(const AttnArgs& a, int d, int mt, bool paged,
+cudaError_t launch_attn_dense(const AttnSkArgs& a, int d, int mt, bool paged,
                               cudaStream_t st);
 int occupancy_attn_sparse(int d, int mt);
 int occupancy_attn_dense(int d, int mt);

@@ -28,7 +28,10 @@ def qkv(b, hq, hkv, d, w, n, seed):
 
 
 # (b, h_q, h_kv, d, w, n, k): 16-row tiles 1..4, two row blocks, d 64/128,
-# ragged n and k, one sequence with many splits, k past the 2048 split cap.
+# ragged n and k; one unit cut into ~70 position splits (sparse) or spread
+# over ~80 CTAs one tile each (dense); k past the 2048-row offset table of
+# one CTA; more units than resident CTAs (dense CTA ranges that hold the end
+# of one unit, whole units and the start of another).
 SHAPES = [
     (1, 4, 2, 64, 4, 256, 32),
     (2, 28, 4, 128, 4, 700, 131),
@@ -38,6 +41,8 @@ SHAPES = [
     (1, 64, 4, 64, 5, 900, 450),
     (1, 8, 1, 128, 3, 5000, 4500),
     (4, 14, 2, 64, 4, 129, 65),
+    (48, 32, 8, 128, 2, 600, 300),
+    (40, 16, 4, 64, 3, 400, 130),
 ]
 
 
@@ -53,7 +58,10 @@ def test_sparse_attention_parity(shape):
     H.assert_attn_close(o, lse, o_ref, lse_ref)
 
 
-@pytest.mark.parametrize("shape", SHAPES[:6], ids=[str(s) for s in SHAPES[:6]])
+DENSE_SHAPES = SHAPES[:6] + SHAPES[8:]
+
+
+@pytest.mark.parametrize("shape", DENSE_SHAPES, ids=[str(s) for s in DENSE_SHAPES])
 def test_full_attention_parity(shape):
     b, hq, hkv, d, w, n, _ = shape
     q, kk, v = qkv(b, hq, hkv, d, w, n, seed=sum(shape) + 1)
@@ -62,6 +70,38 @@ def test_full_attention_parity(shape):
     o_ref, lse_ref = O.full_verify_attention(H.f64(q), H.f64(kk), H.f64(v),
                                              scale)
     H.assert_attn_close(o, lse, o_ref, lse_ref)
+
+
+@pytest.mark.parametrize("shape", [SHAPES[6], SHAPES[8]], ids=["one-unit", "many-units"])
+def test_reused_workspace_gives_identical_results(shape):
+    """Dense units shared between CTAs are merged through per-unit counters
+    kept in the workspace.  A workspace full of 0xff bytes, reused over
+    several calls (sparse and dense alternating), must give bit-identical
+    outputs: the merge order is fixed whichever CTA finishes a unit last."""
+    b, hq, hkv, d, w, n, k = shape
+    q, kk, v = (t.to(DEV) for t in qkv(b, hq, hkv, d, w, n, seed=77))
+    idx = I.random_sorted_indices(b, n, k, seed=78).to(DEV)
+    desc = N.kv_desc(kk, v)
+    nbytes = max(N.dustin_sparse_verify_attn_workspace_size(b, hq, hkv, d, w, k),
+                 N.dustin_full_verify_attn_workspace_size(b, hq, hkv, d, w, n))
+    ws = N.workspace(nbytes, DEV)
+    ws.fill_(255)
+    outs = []
+    for rep in range(3):
+        o = torch.full_like(q, float("nan"))
+        lse = torch.full((b, hq, w), float("nan"), device=DEV)
+        N.dustin_sparse_verify_attn(q, desc, hkv, n, idx, 0.1, o, lse, ws)
+        fo = torch.full_like(q, float("nan"))
+        flse = torch.full((b, hq, w), float("nan"), device=DEV)
+        N.dustin_full_verify_attn(q, desc, hkv, n, 0.1, fo, flse, ws)
+        H.sync()
+        outs.append((o, lse, fo, flse))
+    assert N.dustin_device_status() == 0
+    for later in outs[1:]:
+        assert all(torch.equal(x, y) for x, y in zip(outs[0], later))
+    o_ref, l_ref = O.verify_attention(H.f64(q), H.f64(kk), H.f64(v),
+                                      idx.cpu().numpy(), 0.1)
+    H.assert_attn_close(outs[0][0], outs[0][1], o_ref, l_ref)
 
 
 def test_sparse_with_all_positions_matches_full():

@@ -207,12 +207,16 @@ class Replica:
         self.select = N.prepare_hybrid_topk(
             self.s_d, self.s_t, wl.k, wl.n_sink, wl.n_recent, wl.alpha, wl.m,
             N.DUSTIN_NORM_L1, self.idx)
+        # Layer 0 follows the select kernel, which writes idx; every later
+        # layer follows the previous layer's attention, which writes only its
+        # own outputs, so its K/V gather may start before that one finishes.
+        ready = lambda l: N.DUSTIN_ATTN_KV_READY if l > 0 else 0
         self.attn = [N.prepare_sparse_verify_attn(
             inp.q[l], kv[l], wl.hkv, n, self.idx, wl.scale, self.o[l],
-            self.lse[l], self.ws_a) for l in range(self.L)]
+            self.lse[l], self.ws_a, flags=ready(l)) for l in range(self.L)]
         self.full = [N.prepare_full_verify_attn(
             inp.q[l], kv[l], wl.hkv, n, wl.scale, self.o[l], self.lse[l],
-            self.ws_f) for l in range(self.L)]
+            self.ws_f, flags=ready(l)) for l in range(self.L)]
 
     def step(self, ev=None):
         """One pass of the hot path; ev (optional) records events at the

@@ -210,8 +210,9 @@ int dustin_hybrid_topk(int b, int n, int k, int n_sink, int n_recent,
  *   o    bf16 [b][h_q][w][d], device;  lse fp32 [b][h_q][w] (natural log)
  *   ws   device scratch of dustin_sparse_verify_attn_workspace_size() bytes
  *        (may be 0 bytes; ws may then be NULL)
+ *   flags  0, or DUSTIN_ATTN_KV_READY (below)
  * Limits: d in {64, 128}; h_q a multiple of h_kv; k <= n; scale finite and
- * > 0.
+ * > 0; flags has no other bit set (DUSTIN_ERR_INVALID_ARG).
  */
 size_t dustin_sparse_verify_attn_workspace_size(int b, int h_q, int h_kv,
                                                 int d, int w, int k);
@@ -219,18 +220,32 @@ int dustin_sparse_verify_attn(int b, int h_q, int h_kv, int d, int w, int n,
                               int k, const void* q, const dustin_kv* kv,
                               const int32_t* idx, float scale, void* o,
                               float* lse, void* ws, size_t ws_bytes,
-                              void* stream);
+                              unsigned flags, void* stream);
+
+/* DUSTIN_ATTN_KV_READY: the caller guarantees that idx, the page table and
+ * the K/V cache were complete before the kernel enqueued just before this
+ * call on `stream` started (that kernel does not write them; q may be its
+ * output).  The attention kernels are launched with programmatic dependent
+ * launch and may then gather their first K/V tiles while that kernel is
+ * still running; q is read, and o, lse and ws are written, only after it
+ * has finished.  This holds, for example, for consecutive layers'
+ * verification attention over one index set whose K/V were appended
+ * before the step.  Without the flag nothing is read early.  A wrong
+ * promise gives stale rows, never a fault.  Not an API of the paper: a
+ * launch-overlap hint. */
+#define DUSTIN_ATTN_KV_READY 1u
 
 /* ------------------------------------------------------------------------
  * Full-cache verification attention: the dense in-run baseline ([Notes]
- * section 3, Fig. 7 "Full Cache").  The sparse call over idx = 0..n-1.
+ * section 3, Fig. 7 "Full Cache").  The sparse call over idx = 0..n-1;
+ * flags as there (DUSTIN_ATTN_KV_READY: the page table and K/V).
  */
 size_t dustin_full_verify_attn_workspace_size(int b, int h_q, int h_kv,
                                               int d, int w, int n);
 int dustin_full_verify_attn(int b, int h_q, int h_kv, int d, int w, int n,
                             const void* q, const dustin_kv* kv, float scale,
                             void* o, float* lse, void* ws, size_t ws_bytes,
-                            void* stream);
+                            unsigned flags, void* stream);
 
 #ifdef __cplusplus
 }

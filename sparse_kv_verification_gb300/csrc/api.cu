@@ -222,7 +222,7 @@ int check_attn_shape(int b, int hq, int hkv, int d, int w, int n,
 int run_attn(bool dense, int b, int hq, int hkv, int d, int w, int n, int k,
              const void* q, const dustin_kv* kv, const int32_t* idx,
              float scale, void* o, float* lse, void* ws, size_t ws_bytes,
-             void* stream) {
+             unsigned flags, void* stream) {
   const char* what = dense ? "dustin_full_verify_attn" : "dustin_sparse_verify_attn";
   int rc = check_attn_shape(b, hq, hkv, d, w, n, what);
   if (rc) return rc;
@@ -240,6 +240,8 @@ int run_attn(bool dense, int b, int hq, int hkv, int d, int w, int n, int k,
                 what);
   if (!std::isfinite(scale) || !(scale > 0.f))
     return fail(DUSTIN_ERR_INVALID_ARG, "%s: scale must be finite and > 0", what);
+  if (flags & ~DUSTIN_ATTN_KV_READY)
+    return fail(DUSTIN_ERR_INVALID_ARG, "%s: unknown flags 0x%x", what, flags);
   rc = check_kv(kv, b, n, d, true, what);
   if (rc) return rc;
   const bool paged = kv->page_table != nullptr;
@@ -271,6 +273,7 @@ int run_attn(bool dense, int b, int hq, int hkv, int d, int w, int n, int k,
     a.splits = p.splits;
     a.chunk = p.chunk;
     a.scale_log2 = scale * kLog2e;
+    a.kv_ready = (flags & DUSTIN_ATTN_KV_READY) ? 1 : 0;
     a.ws_o = need ? static_cast<float*>(ws) : nullptr;
     a.ws_ml = need ? reinterpret_cast<float2*>(static_cast<char*>(ws) + p.ws_o)
                    : nullptr;
@@ -304,6 +307,7 @@ int run_attn(bool dense, int b, int hq, int hkv, int d, int w, int n, int k,
     a.tpu = p.tpu;
     a.grid = (int)p.grid;
     a.scale_log2 = scale * kLog2e;
+    a.kv_ready = (flags & DUSTIN_ATTN_KV_READY) ? 1 : 0;
     char* wsb = static_cast<char*>(ws);
     a.ws_o = need ? reinterpret_cast<float*>(wsb) : nullptr;
     a.ws_ml = need ? reinterpret_cast<float2*>(wsb + p.ws_o) : nullptr;
@@ -495,9 +499,9 @@ int dustin_sparse_verify_attn(int b, int h_q, int h_kv, int d, int w, int n,
                               int k, const void* q, const dustin_kv* kv,
                               const int32_t* idx, float scale, void* o,
                               float* lse, void* ws, size_t ws_bytes,
-                              void* stream) {
+                              unsigned flags, void* stream) {
   return run_attn(false, b, h_q, h_kv, d, w, n, k, q, kv, idx, scale, o, lse, ws,
-                  ws_bytes, stream);
+                  ws_bytes, flags, stream);
 }
 
 size_t dustin_full_verify_attn_workspace_size(int b, int h_q, int h_kv, int d,
@@ -511,9 +515,9 @@ size_t dustin_full_verify_attn_workspace_size(int b, int h_q, int h_kv, int d,
 int dustin_full_verify_attn(int b, int h_q, int h_kv, int d, int w, int n,
                             const void* q, const dustin_kv* kv, float scale,
                             void* o, float* lse, void* ws, size_t ws_bytes,
-                            void* stream) {
+                            unsigned flags, void* stream) {
   return run_attn(true, b, h_q, h_kv, d, w, n, n, q, kv, nullptr, scale, o, lse,
-                  ws, ws_bytes, stream);
+                  ws, ws_bytes, flags, stream);
 }
 
 }  // extern "C"

@@ -62,6 +62,7 @@ struct AttnArgs {
   int splits;
   int chunk;        // positions per split (multiple of 64)
   float scale_log2; // scale * log2(e)
+  int kv_ready;     // idx, page table and K/V may be read before the wait
   float* ws_o;      // [blocks][splits][16 MT][D] (splits > 1)
   float2* ws_ml;    // [blocks][splits][16 MT]    (m in log2 units, l)
 };
@@ -172,17 +173,30 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
       ((long long)bb * a.hq + (long long)g * a.group) * a.w;  // first q row
   const int r_lo = rb * C::ROWS;
 
-  griddep_wait();
-  griddep_launch_dependents();
+  // Programmatic dependent launch: the kernel before this one on the stream
+  // may still be running until griddepcontrol.wait returns.  Normally every
+  // thread waits first.  With kv_ready the caller guarantees that idx, the
+  // page table and K/V were not written by that kernel: the table is built
+  // and the first STAGES tiles are fetched before the wait, and only q (and
+  // every write) waits.  A thread triggers the next launch only after its
+  // own wait, so a kernel never starts early while its predecessor's
+  // predecessor may still be running.
+  if (!a.kv_ready) {
+    griddep_wait();
+    griddep_launch_dependents();
+  }
 
   // ---- Q rows into shared memory (zero rows past G*w), barriers.
-  for (int c = tid; c < C::ROWS * C::CPR; c += C::NT) {
-    const int r = c / C::CPR, ch = c % C::CPR;
-    const int R = r_lo + r;
-    const bool ok = R < a.rows;
-    cp_async_16(smem_u32(sQ + r * C::RS + ch * 16),
-                a.q + (ok ? (row_base + R) * D + ch * 8 : 0), ok ? 16 : 0);
-  }
+  auto load_q = [&](int first, int step) {
+    for (int c = first; c < C::ROWS * C::CPR; c += step) {
+      const int r = c / C::CPR, ch = c % C::CPR;
+      const int R = r_lo + r;
+      const bool ok = R < a.rows;
+      cp_async_16(smem_u32(sQ + r * C::RS + ch * 16),
+                  a.q + (ok ? (row_base + R) * D + ch * 8 : 0), ok ? 16 : 0);
+    }
+  };
+  if (!a.kv_ready) load_q(tid, C::NT);
   cp_async_commit();
   if (tid == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -242,8 +256,18 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
       return i < len ? tab[i] : -1;
     };
 
+    // kv_ready: the first n_pre tiles go out before this thread's wait.
+    const int n_pre = a.kv_ready ? min(ntiles, C::STAGES) : -1;
+    if (n_pre == 0) {
+      griddep_wait();
+      griddep_launch_dependents();
+    }
     for (int t = 0; t < ntiles; ++t) {
       const int s = t % C::STAGES;
+      if (t == n_pre) {
+        griddep_wait();
+        griddep_launch_dependents();
+      }
       if (t >= C::STAGES &&
           !mbar_wait(empty_bar(s), ((t / C::STAGES) & 1) ^ 1, kWaitLimitCycles)) {
         if (lane == 0) atomicOr(&g_attn_dev_flags, 4u);
@@ -279,6 +303,10 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
         mbar_arrive(full_bar(s));
       }
     }
+    if (n_pre == ntiles && ntiles > 0) {   // every tile went out early
+      griddep_wait();
+      griddep_launch_dependents();
+    }
     // Every copy of this thread lands before the CTA may exit.
     cp_async_wait<0>();
     return;
@@ -289,6 +317,14 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(C::CONSUMER_REGS));
   const int wm = warp / C::WN;
   const int wn = warp % C::WN;
+  if (a.kv_ready) {
+    griddep_wait();
+    griddep_launch_dependents();
+    load_q(tid, C::NCW * 32);
+    cp_async_commit();
+    cp_async_wait<0>();
+    named_bar_sync(1, C::NCW * 32);
+  }
   uint32_t qf[C::KS][4];
 #pragma unroll
   for (int ks = 0; ks < C::KS; ++ks) {

@@ -58,6 +58,7 @@ struct AttnSkArgs {
   int tpu;          // tiles per unit: max(1, ceil(n / 64))
   int grid;         // CTAs (G)
   float scale_log2; // scale * log2(e)
+  int kv_ready;     // the page table and K/V may be read before the wait
   float* ws_o;      // [2 G][16 MT][D] partial O   (when some unit is split)
   float2* ws_ml;    // [2 G][16 MT] (m in log2 units, l)
   unsigned long long* counters;  // [units] (epoch << 24 | count)
@@ -208,8 +209,15 @@ __global__ void __launch_bounds__(SkCfg<D, MT>::NT, 1)
     lt1 = (int)(min(r1, ub + a.tpu) - ub);
   };
 
-  griddep_wait();
-  griddep_launch_dependents();
+  // Programmatic dependent launch, as in the sparse kernel: normally every
+  // thread waits for the previous kernel first; with kv_ready the page
+  // table and the first STAGES tiles are fetched before the wait, and only
+  // q (and every write) waits.  A thread triggers the next launch only after
+  // its own wait.
+  if (!a.kv_ready) {
+    griddep_wait();
+    griddep_launch_dependents();
+  }
 
   // ---- Query rows of a unit into shared memory (zero past G*w).
   auto load_q = [&](int u, int first, int step) {
@@ -222,7 +230,7 @@ __global__ void __launch_bounds__(SkCfg<D, MT>::NT, 1)
                   a.q + (ok ? (x.row_base + R) * D + ch * 8 : 0), ok ? 16 : 0);
     }
   };
-  if (nseg > 0) load_q(u_first, tid, C::NT);
+  if (nseg > 0 && !a.kv_ready) load_q(u_first, tid, C::NT);
   cp_async_commit();
   if (tid == 0) {
     sRange[0] = T0;
@@ -314,6 +322,14 @@ __global__ void __launch_bounds__(SkCfg<D, MT>::NT, 1)
 
     int t = 0;   // tile counter over the whole range (stage, phase)
     bool ok_run = true;
+    bool waited = !a.kv_ready;   // kv_ready: wait after the first STAGES tiles
+    auto ensure_wait = [&]() {
+      if (!waited) {
+        griddep_wait();
+        griddep_launch_dependents();
+        waited = true;
+      }
+    };
     for (int s = 0; s < nseg && ok_run; ++s) {
       int u, lt0, lt1;
       seg_range(s, u, lt0, lt1);
@@ -321,6 +337,7 @@ __global__ void __launch_bounds__(SkCfg<D, MT>::NT, 1)
       long long kv_off = 0;
       if constexpr (!PAGED) kv_off = unit_of(u).kv_off;
       if (s > 0) {
+        ensure_wait();
         // The consumers took the previous query rows into registers.
         if (!mbar_wait(q_empty, (s - 1) & 1, kWaitLimitCycles)) {
           if (lane == 0) atomicOr(&g_attn_sk_dev_flags, 4u);
@@ -331,6 +348,7 @@ __global__ void __launch_bounds__(SkCfg<D, MT>::NT, 1)
       }
       for (int lt = lt0; lt < lt1; ++lt, ++t) {
         const int st = t % C::STAGES;
+        if (t >= C::STAGES) ensure_wait();
         if (t >= C::STAGES &&
             !mbar_wait(empty_bar(st), ((t / C::STAGES) & 1) ^ 1, kWaitLimitCycles)) {
           if (lane == 0) atomicOr(&g_attn_sk_dev_flags, 4u);
@@ -372,6 +390,7 @@ __global__ void __launch_bounds__(SkCfg<D, MT>::NT, 1)
         }
       }
     }
+    ensure_wait();
     // Every copy of this thread lands before the CTA may exit.
     cp_async_wait<0>();
     return;
@@ -382,6 +401,14 @@ __global__ void __launch_bounds__(SkCfg<D, MT>::NT, 1)
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(C::CONSUMER_REGS));
   const int wm = warp / C::WN;
   const int wn = warp % C::WN;
+  if (a.kv_ready) {
+    griddep_wait();
+    griddep_launch_dependents();
+    if (nseg > 0) load_q(u_first, tid, C::NCW * 32);
+    cp_async_commit();
+    cp_async_wait<0>();
+    named_bar_sync(1, C::NCW * 32);
+  }
   const int gq = lane >> 2, tq = lane & 3;
   int t = 0;
   bool dead = false;

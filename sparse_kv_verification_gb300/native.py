@@ -18,6 +18,7 @@ from . import build as _build
 DUSTIN_OK = 0
 DUSTIN_NORM_NONE = 0
 DUSTIN_NORM_L1 = 1
+DUSTIN_ATTN_KV_READY = 1
 
 EXPORTS = (
     "dustin_status_string", "dustin_last_error", "dustin_version",
@@ -73,8 +74,8 @@ def load(build_if_missing: bool = False, path: Optional[str] = None
                 "`python -m sparse_kv_verification_gb300.build`")
         _build.build()
     lib = ctypes.CDLL(path)
-    P, I, F, D, S = (ctypes.c_void_p, ctypes.c_int, ctypes.c_float,
-                     ctypes.c_double, ctypes.c_size_t)
+    P, I, F, D, S, U = (ctypes.c_void_p, ctypes.c_int, ctypes.c_float,
+                        ctypes.c_double, ctypes.c_size_t, ctypes.c_uint)
     sig = {
         "dustin_status_string": (ctypes.c_char_p, [I]),
         "dustin_last_error": (ctypes.c_char_p, []),
@@ -87,10 +88,10 @@ def load(build_if_missing: bool = False, path: Optional[str] = None
         "dustin_hybrid_topk": (I, [I, I, I, I, I, D, I, I, P, P, P, P]),
         "dustin_sparse_verify_attn_workspace_size": (S, [I, I, I, I, I, I]),
         "dustin_sparse_verify_attn": (I, [I, I, I, I, I, I, I, P, P, P, F, P, P,
-                                          P, S, P]),
+                                          P, S, U, P]),
         "dustin_full_verify_attn_workspace_size": (S, [I, I, I, I, I, I]),
         "dustin_full_verify_attn": (I, [I, I, I, I, I, I, P, P, F, P, P, P, S,
-                                        P]),
+                                        U, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -255,7 +256,8 @@ def _attn_checks(q, o, lse):
 def dustin_sparse_verify_attn(q: torch.Tensor, kv: DustinKV, h_kv: int,
                               n: int, idx: torch.Tensor, scale: float,
                               o: torch.Tensor, lse: torch.Tensor,
-                              ws: Optional[torch.Tensor], stream=None) -> None:
+                              ws: Optional[torch.Tensor], stream=None,
+                              flags: int = 0) -> None:
     _attn_checks(q, o, lse)
     b, h_q, w, d = q.shape
     if idx.dtype != torch.int32 or not idx.is_contiguous() or idx.dim() != 2 \
@@ -265,18 +267,20 @@ def dustin_sparse_verify_attn(q: torch.Tensor, kv: DustinKV, h_kv: int,
     _check(load().dustin_sparse_verify_attn(
         b, h_q, h_kv, d, w, n, k, q.data_ptr(), ctypes.byref(kv),
         idx.data_ptr(), float(scale), o.data_ptr(), lse.data_ptr(),
-        _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream, q.device)))
+        _ptr(ws), 0 if ws is None else ws.numel(), int(flags),
+        _stream(stream, q.device)))
 
 
 def dustin_full_verify_attn(q: torch.Tensor, kv: DustinKV, h_kv: int, n: int,
                             scale: float, o: torch.Tensor, lse: torch.Tensor,
-                            ws: Optional[torch.Tensor], stream=None) -> None:
+                            ws: Optional[torch.Tensor], stream=None,
+                            flags: int = 0) -> None:
     _attn_checks(q, o, lse)
     b, h_q, w, d = q.shape
     _check(load().dustin_full_verify_attn(
         b, h_q, h_kv, d, w, n, q.data_ptr(), ctypes.byref(kv), float(scale),
         o.data_ptr(), lse.data_ptr(), _ptr(ws), 0 if ws is None else ws.numel(),
-        _stream(stream, q.device)))
+        int(flags), _stream(stream, q.device)))
 
 
 # ------------------------------------------------------------------ misc
@@ -329,7 +333,7 @@ def prepare_hybrid_topk(s_draft, s_target, k, n_sink, n_recent, alpha, m,
 
 
 def prepare_sparse_verify_attn(q, kv, h_kv, n, idx, scale, o, lse, ws,
-                               stream=None):
+                               stream=None, flags=0):
     _attn_checks(q, o, lse)
     b, h_q, w, d = q.shape
     fn = load().dustin_sparse_verify_attn
@@ -337,7 +341,7 @@ def prepare_sparse_verify_attn(q, kv, h_kv, n, idx, scale, o, lse, ws,
     args = (b, h_q, h_kv, d, w, n, idx.shape[1], q.data_ptr(),
             ctypes.addressof(kvc), idx.data_ptr(), float(scale), o.data_ptr(),
             lse.data_ptr(), _ptr(ws), 0 if ws is None else ws.numel(),
-            _stream(stream, q.device))
+            int(flags), _stream(stream, q.device))
 
     def call():
         _check(fn(*args))
@@ -345,14 +349,15 @@ def prepare_sparse_verify_attn(q, kv, h_kv, n, idx, scale, o, lse, ws,
     return call
 
 
-def prepare_full_verify_attn(q, kv, h_kv, n, scale, o, lse, ws, stream=None):
+def prepare_full_verify_attn(q, kv, h_kv, n, scale, o, lse, ws, stream=None,
+                             flags=0):
     _attn_checks(q, o, lse)
     b, h_q, w, d = q.shape
     fn = load().dustin_full_verify_attn
     kvc = DustinKV.from_buffer_copy(kv)
     args = (b, h_q, h_kv, d, w, n, q.data_ptr(), ctypes.addressof(kvc),
             float(scale), o.data_ptr(), lse.data_ptr(), _ptr(ws),
-            0 if ws is None else ws.numel(), _stream(stream, q.device))
+            0 if ws is None else ws.numel(), int(flags), _stream(stream, q.device))
 
     def call():
         _check(fn(*args))

@@ -62,13 +62,13 @@ def kv(stride_n=128, d=128, page_table=None, page_size=0, ppseq=0, pages=0,
 def sparse(lib, **kw):
     args = dict(b=1, hq=8, hkv=2, d=128, w=4, n=256, k=32, q=FAKE,
                 kv=kv(), idx=FAKE, scale=0.1, o=FAKE, lse=FAKE, ws=None,
-                ws_bytes=0)
+                ws_bytes=0, flags=0)
     args.update(kw)
     r = lib.dustin_sparse_verify_attn(
         args["b"], args["hq"], args["hkv"], args["d"], args["w"], args["n"],
         args["k"], args["q"], ctypes.byref(args["kv"]), args["idx"],
         args["scale"], args["o"], args["lse"], args["ws"], args["ws_bytes"],
-        None)
+        args["flags"], None)
     return r, lib.dustin_last_error().decode()
 
 
@@ -87,6 +87,7 @@ def test_attention_validation(lib):
     assert sparse(lib, scale=float("nan"))[0] == 1
     assert sparse(lib, scale=0.0)[0] == 1
     assert sparse(lib, scale=-0.5)[0] == 1
+    assert sparse(lib, flags=2)[0] == 1           # unknown flag bit
     assert sparse(lib, kv=kv(page_table=FAKE, page_size=8, ppseq=32,
                              pages=64))[0] == 3
     assert sparse(lib, kv=kv(page_table=FAKE, page_size=16, ppseq=4,

@@ -104,6 +104,55 @@ def test_reused_workspace_gives_identical_results(shape):
     H.assert_attn_close(outs[0][0], outs[0][1], o_ref, l_ref)
 
 
+@pytest.mark.parametrize("case", ["contiguous", "paged", "split"])
+def test_kv_ready_launch_overlap_gives_identical_results(case):
+    """DUSTIN_ATTN_KV_READY lets a launch gather K/V while the kernel before
+    it on the stream still runs.  Consecutive layers over one index set
+    (layer 0 after a kernel that writes idx, so without the flag), back to
+    back on one stream, must give the same bits as calls without it."""
+    b, hq, hkv, d, w, n, k = {"contiguous": (4, 32, 4, 128, 5, 3000, 700),
+                              "paged": (2, 16, 2, 128, 4, 1000, 300),
+                              "split": (1, 8, 1, 128, 3, 5000, 4500)}[case]
+    layers = 4
+    idx = I.random_sorted_indices(b, n, k, seed=21).to(DEV)
+    qs, descs, keep = [], [], []
+    for l in range(layers):
+        q, kk, v = qkv(b, hq, hkv, d, w, n, seed=100 + l)
+        if case == "paged":
+            kk, v, table = I.to_paged(kk, v, 16, seed=200 + l)
+            table = table.to(DEV)
+        else:
+            table = None
+        q, kk, v = q.to(DEV), kk.to(DEV), v.to(DEV)
+        keep += [kk, v, table]
+        qs.append(q)
+        descs.append(N.kv_desc(kk, v, table))
+    ws_s = N.workspace(N.dustin_sparse_verify_attn_workspace_size(b, hq, hkv, d, w, k), DEV)
+    ws_f = N.workspace(N.dustin_full_verify_attn_workspace_size(b, hq, hkv, d, w, n), DEV)
+
+    def run(ready):
+        outs = []
+        for dense in (False, True):
+            for l in range(layers):
+                o = torch.full_like(qs[l], float("nan"))
+                lse = torch.full((b, hq, w), float("nan"), device=DEV)
+                flags = N.DUSTIN_ATTN_KV_READY if ready and l > 0 else 0
+                if dense:
+                    N.dustin_full_verify_attn(qs[l], descs[l], hkv, n, 0.1, o, lse,
+                                              ws_f, flags=flags)
+                else:
+                    N.dustin_sparse_verify_attn(qs[l], descs[l], hkv, n, idx, 0.1,
+                                                o, lse, ws_s, flags=flags)
+                outs.append((o, lse))
+        H.sync()
+        return outs
+
+    plain, ready = run(False), run(True)
+    assert N.dustin_device_status() == 0
+    for (o1, l1), (o2, l2) in zip(plain, ready):
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
 def test_sparse_with_all_positions_matches_full():
     b, hq, hkv, d, w, n = 2, 16, 2, 128, 4, 777
     q, kk, v = qkv(b, hq, hkv, d, w, n, seed=5)

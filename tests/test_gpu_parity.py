@@ -271,6 +271,12 @@ SELECT_CASES = [
     (1, 1, 1, 0, 0, 0.5, -1, 1, False),
     (3, 17, 5, 0, 0, 0.5, -1, 1, False),
     (2, 65536, 8192, 4, 64, 0.5, -1, 1, True),
+    # one 8-CTA cluster per sequence: m mode, ragged segments, and rows too
+    # long for the keys to stay in shared memory
+    (2, 32768, 2048, 4, 64, 0.5, 512, 1, True),
+    (2, 12345, 1500, 3, 17, 0.3, -1, 1, True),
+    (1, 400000, 4000, 4, 64, 0.5, -1, 1, False),
+    (1, 400000, 4000, 4, 64, 0.5, 1000, 1, False),
 ]
 
 
@@ -282,6 +288,19 @@ def test_select_bit_exact(case):
     got = H.select(sd.to(DEV), st.to(DEV), k, ns, nr, alpha, m, norm)
     want = O.hybrid_select(sd.numpy(), st.numpy(), k, ns, nr, alpha, m, norm)
     np.testing.assert_array_equal(got.cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("n", [32768, 20000])
+def test_select_ties_across_the_cluster(n):
+    """Equal scores spread over every CTA of a sequence's cluster: the tie
+    rule (lower position first) must hold across CTA boundaries."""
+    g = I.generator(n)
+    sd = torch.where(torch.rand((2, n), generator=g) < 0.5, 1.0, 0.5).float()
+    st = torch.ones((2, n))
+    for k in (1000, n // 2 + 7, n - 100):
+        got = H.select(sd.to(DEV), st.to(DEV), k, 4, 64, 0.5, -1, 1)
+        want = O.hybrid_select(sd.numpy(), st.numpy(), k, 4, 64, 0.5, -1, 1)
+        np.testing.assert_array_equal(got.cpu().numpy(), want)
 
 
 def test_select_single_vector():

@@ -300,6 +300,47 @@ def verify_attention(q: np.ndarray, keys: np.ndarray, values: np.ndarray,
     return out, lse
 
 
+def verify_attention_window(q: np.ndarray, keys: np.ndarray,
+                            values: np.ndarray, idx: Optional[np.ndarray],
+                            k_win: np.ndarray, v_win: np.ndarray, scale: float
+                            ) -> Tuple[np.ndarray, np.ndarray]:
+    """Verification attention of the w window rows over the selected history
+    and, causally, over the window itself ([Notes] section 2.2 Fig. 5,
+    Stage 2: the target scores its w draft positions in one pass; the draft
+    tokens follow the history, so row t sees every selected history position
+    and the window positions 0..t, as in ordinary causal decoding).
+
+    q [b][hq][w][d]; keys, values [b][hkv][n][d]; idx [b][k] (None: all n);
+    k_win, v_win [b][hkv][w][d], the window tokens' own keys and values.
+    For row t of head h (kv head g = h // (hq // hkv)):
+      logits = scale * q . [K[g][idx], K_win[g][0..t]]
+      O = softmax(logits) [V[g][idx], V_win[g][0..t]],  LSE = log sum exp.
+    Returns (O [b][hq][w][d], LSE [b][hq][w]) in float64."""
+    q = np.asarray(q, np.float64)
+    keys = np.asarray(keys, np.float64)
+    values = np.asarray(values, np.float64)
+    k_win = np.asarray(k_win, np.float64)
+    v_win = np.asarray(v_win, np.float64)
+    b, hq, w, d = q.shape
+    hkv = keys.shape[1]
+    group = hq // hkv
+    out = np.zeros((b, hq, w, d), dtype=np.float64)
+    lse = np.zeros((b, hq, w), dtype=np.float64)
+    for bi in range(b):
+        sel = np.arange(keys.shape[2]) if idx is None else \
+            np.asarray(idx[bi], dtype=np.int64)
+        for h in range(hq):
+            g = h // group
+            for t in range(w):
+                kk = np.concatenate([keys[bi, g][sel], k_win[bi, g, :t + 1]])
+                vv = np.concatenate([values[bi, g][sel], v_win[bi, g, :t + 1]])
+                logits = scale * (kk @ q[bi, h, t])
+                p = softmax(logits)
+                out[bi, h, t] = p @ vv
+                lse[bi, h, t] = logsumexp(logits)
+    return out, lse
+
+
 def full_verify_attention(q, keys, values, scale):
     """Full-cache verification (the dense baseline of [Notes] section 3,
     Fig. 7): ``verify_attention`` over every history position."""

@@ -148,6 +148,84 @@ def test_sparse_attention_is_dense_attention_on_gathered_cache():
     np.testing.assert_array_equal(l1, l2)
 
 
+# ------------------------------------------------ window self-block merged in
+
+def _window_case(seed, b=2, hq=4, hkv=2, w=4, n=40, d=16, k=9):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((b, hq, w, d))
+    kk = rng.standard_normal((b, hkv, n, d))
+    vv = rng.standard_normal((b, hkv, n, d))
+    kw = rng.standard_normal((b, hkv, w, d))
+    vw = rng.standard_normal((b, hkv, w, d))
+    idx = np.stack([np.sort(rng.choice(n, k, replace=False)) for _ in range(b)])
+    return q, kk, vv, kw, vw, idx
+
+
+def test_window_attention_matches_sdpa_with_a_causal_window_mask():
+    """Library special case: SDPA in fp64 over [K[idx]; K_win] with a mask
+    that opens all the selected history and the causal part of the window."""
+    q, kk, vv, kw, vw, idx = _window_case(21)
+    b, hq, w, d = q.shape
+    group = hq // kk.shape[1]
+    o, lse = O.verify_attention_window(q, kk, vv, idx, kw, vw, 0.3)
+    for bi in range(b):
+        ck = np.concatenate([kk[bi][:, idx[bi]], kw[bi]], axis=1)
+        cv = np.concatenate([vv[bi][:, idx[bi]], vw[bi]], axis=1)
+        tk = torch.from_numpy(ck).repeat_interleave(group, dim=0)[None]
+        tv = torch.from_numpy(cv).repeat_interleave(group, dim=0)[None]
+        kk_len = idx.shape[1]
+        mask = torch.ones((w, kk_len + w), dtype=torch.bool)
+        mask[:, kk_len:] = torch.tril(torch.ones((w, w), dtype=torch.bool))
+        tq = torch.from_numpy(q[bi:bi + 1])
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            tq, tk, tv, attn_mask=mask, scale=0.3)
+        np.testing.assert_allclose(o[bi:bi + 1], ref.numpy(), atol=1e-12)
+        logits = 0.3 * (tq @ tk.transpose(-1, -2))
+        ref_lse = torch.logsumexp(logits.masked_fill(~mask, -math.inf), dim=-1)
+        np.testing.assert_allclose(lse[bi:bi + 1], ref_lse.numpy(), atol=1e-12)
+
+
+def test_window_attention_without_history_is_causal_self_attention():
+    q, kk, vv, kw, vw, _ = _window_case(22)
+    group = q.shape[1] // kk.shape[1]
+    empty = np.zeros((q.shape[0], 0), dtype=np.int64)
+    o, _ = O.verify_attention_window(q, kk, vv, empty, kw, vw, 0.25)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q),
+        torch.from_numpy(kw).repeat_interleave(group, dim=1),
+        torch.from_numpy(vw).repeat_interleave(group, dim=1),
+        is_causal=True, scale=0.25)
+    np.testing.assert_allclose(o, ref.numpy(), atol=1e-12)
+
+
+def test_window_attention_is_the_lse_merge_of_history_and_window():
+    """Splitting the softmax over a disjoint union: the joint output is the
+    two parts' outputs weighted by exp(LSE) (closed form)."""
+    q, kk, vv, kw, vw, idx = _window_case(23)
+    o, lse = O.verify_attention_window(q, kk, vv, idx, kw, vw, 0.4)
+    o_h, l_h = O.verify_attention(q, kk, vv, idx, 0.4)
+    b, hq, w, d = q.shape
+    group = hq // kk.shape[1]
+    for bi in range(b):
+        for h in range(hq):
+            g = h // group
+            for t in range(w):
+                lw = 0.4 * (kw[bi, g, :t + 1] @ q[bi, h, t])
+                l_w = scipy.special.logsumexp(lw)
+                o_w = scipy.special.softmax(lw) @ vw[bi, g, :t + 1]
+                m = max(l_h[bi, h, t], l_w)
+                a_h, a_w = math.exp(l_h[bi, h, t] - m), math.exp(l_w - m)
+                np.testing.assert_allclose(
+                    o[bi, h, t], (a_h * o_h[bi, h, t] + a_w * o_w) / (a_h + a_w),
+                    atol=1e-12)
+                assert lse[bi, h, t] == pytest.approx(
+                    m + math.log(a_h + a_w), abs=1e-12)
+    # w = 1: the single row sees the history and itself.
+    o1, _ = O.verify_attention_window(q[:, :, :1], kk, vv, idx, kw[:, :, :1],
+                                      vw[:, :, :1], 0.4)
+    np.testing.assert_allclose(o1, o[:, :, :1], atol=1e-12)
+
+
 def test_attention_closed_forms():
     rng = np.random.default_rng(13)
     d, n = 8, 20

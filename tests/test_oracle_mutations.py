@@ -74,6 +74,26 @@ def _softmax_transposed(logits):
     return e / np.sum(e, axis=-2, keepdims=True)
 
 
+def _window_attention_not_causal(q, keys, values, idx, k_win, v_win, scale):
+    # the window rows see the whole window, later tokens included
+    q = np.asarray(q, np.float64)
+    b, hq, w, d = q.shape
+    group = hq // np.asarray(keys).shape[1]
+    out = np.zeros((b, hq, w, d))
+    lse = np.zeros((b, hq, w))
+    for bi in range(b):
+        sel = np.arange(keys.shape[2]) if idx is None else np.asarray(idx[bi])
+        for h in range(hq):
+            g = h // group
+            kk = np.concatenate([keys[bi, g][sel], k_win[bi, g]])
+            vv = np.concatenate([values[bi, g][sel], v_win[bi, g]])
+            for t in range(w):
+                logits = scale * (kk @ q[bi, h, t])
+                out[bi, h, t] = O.softmax(logits) @ vv
+                lse[bi, h, t] = O.logsumexp(logits)
+    return out, lse
+
+
 ORIG = {name: getattr(O, name) for name in (
     "score_heads", "hybrid_scores", "softmax")}
 
@@ -94,6 +114,9 @@ MUTATIONS = [
      [pins.test_attention_closed_forms]),
     ("verify_attention", _verify_attention_wrong_gqa,
      [pins.test_gqa_head_mapping]),
+    ("verify_attention_window", _window_attention_not_causal,
+     [pins.test_window_attention_matches_sdpa_with_a_causal_window_mask,
+      pins.test_window_attention_without_history_is_causal_self_attention]),
     ("softmax", _softmax_transposed,
      [lambda: pins.test_dense_attention_matches_torch_sdpa(2, 4, 2, 3, 37, 16)]),
 ]

@@ -222,6 +222,24 @@ int dustin_sparse_verify_attn(int b, int h_q, int h_kv, int d, int w, int n,
                               float* lse, void* ws, size_t ws_bytes,
                               unsigned flags, void* stream);
 
+/* The same with the window's own causal block merged in (the w window
+ * tokens follow the history, so window row t also attends to window
+ * positions 0..t, as in ordinary causal decoding):
+ *   o[b][h][t] = softmax over [idx[b][0..k), window 0..t] of scale * q . K
+ *   lse        = log sum exp over the same positions
+ * where the window part reads win (k and v both required, contiguous, no
+ * page table): bf16 [b][h_kv][w][d] through win->stride_b/h/n.  Same
+ * workspace as dustin_sparse_verify_attn.  With DUSTIN_ATTN_KV_READY the
+ * window rows, like q, are read only after the preceding kernel finished.
+ * (The sparse call's LSE lets a caller merge this block itself; this entry
+ * point does it inside the same launch, as one more tile of w rows.) */
+int dustin_sparse_verify_attn_window(int b, int h_q, int h_kv, int d, int w,
+                                     int n, int k, const void* q,
+                                     const dustin_kv* kv, const int32_t* idx,
+                                     const dustin_kv* win, float scale, void* o,
+                                     float* lse, void* ws, size_t ws_bytes,
+                                     unsigned flags, void* stream);
+
 /* DUSTIN_ATTN_KV_READY: the caller guarantees that idx, the page table and
  * the K/V cache were complete before the kernel enqueued just before this
  * call on `stream` started (that kernel does not write them; q may be its
@@ -246,6 +264,14 @@ int dustin_full_verify_attn(int b, int h_q, int h_kv, int d, int w, int n,
                             const void* q, const dustin_kv* kv, float scale,
                             void* o, float* lse, void* ws, size_t ws_bytes,
                             unsigned flags, void* stream);
+/* The full-cache call with the window's causal block merged in, as
+ * dustin_sparse_verify_attn_window.  dustin_full_verify_attn_workspace_size
+ * covers both. */
+int dustin_full_verify_attn_window(int b, int h_q, int h_kv, int d, int w, int n,
+                                   const void* q, const dustin_kv* kv,
+                                   const dustin_kv* win, float scale, void* o,
+                                   float* lse, void* ws, size_t ws_bytes,
+                                   unsigned flags, void* stream);
 
 #ifdef __cplusplus
 }

@@ -114,7 +114,7 @@ int check_kv(const dustin_kv* kv, int b, int n, int d, bool need_v,
 // Shared by both kernels: a unit is (sequence, kv head, row block of at
 // most 64 query rows, in 16-row tiles).
 struct AttnPlan {
-  int mt, row_blocks, tpu;
+  int mt, row_blocks, tpu, tph;
   long long units;
   // sparse: positions split `splits` ways, `chunk` positions each.
   int splits, chunk;
@@ -167,8 +167,11 @@ AttnPlan plan_sparse(int b, int hq, int hkv, int d, int w, int k) {
 
 // Dense: stream-K over tiles.  G is the number of CTAs resident at once,
 // raised where a CTA's range would overflow its page table (512 tiles).
-AttnPlan plan_dense(int b, int hq, int hkv, int d, int w, int n) {
+AttnPlan plan_dense(int b, int hq, int hkv, int d, int w, int n, bool win) {
   AttnPlan p = plan_units(hq, hkv, w, b, n);
+  // History tiles, then (with the window merged in) one window tile.
+  p.tph = (n + 63) / 64;
+  p.tpu = std::max(1, p.tph + (win ? 1 : 0));
   const long long T = p.units * p.tpu;
   if (T <= 0) return p;
   long long slots = (long long)attn_slots(true, d, p.mt);
@@ -219,11 +222,29 @@ int check_attn_shape(int b, int hq, int hkv, int d, int w, int n,
   return DUSTIN_OK;
 }
 
+// The window's own K/V: [b][h_kv][w][d] through a contiguous descriptor.
+int check_win(const dustin_kv* win, int d, const char* what) {
+  if (!win->k || !win->v)
+    return fail(DUSTIN_ERR_INVALID_ARG, "%s: win.k and win.v are required", what);
+  if (!aligned16(win->k) || !aligned16(win->v))
+    return fail(DUSTIN_ERR_ALIGNMENT, "%s: win base not 16-byte aligned", what);
+  if (win->page_table)
+    return fail(DUSTIN_ERR_UNSUPPORTED, "%s: the window cannot be paged", what);
+  if (win->stride_b < 0 || win->stride_h < 0 || win->stride_n < d)
+    return fail(DUSTIN_ERR_SHAPE, "%s: bad win strides", what);
+  if (win->stride_b % 8 || win->stride_h % 8 || win->stride_n % 8)
+    return fail(DUSTIN_ERR_ALIGNMENT,
+                "%s: win strides must be multiples of 8 elements", what);
+  return DUSTIN_OK;
+}
+
 int run_attn(bool dense, int b, int hq, int hkv, int d, int w, int n, int k,
              const void* q, const dustin_kv* kv, const int32_t* idx,
-             float scale, void* o, float* lse, void* ws, size_t ws_bytes,
-             unsigned flags, void* stream) {
-  const char* what = dense ? "dustin_full_verify_attn" : "dustin_sparse_verify_attn";
+             const dustin_kv* win, float scale, void* o, float* lse, void* ws,
+             size_t ws_bytes, unsigned flags, void* stream) {
+  const char* what = dense ? (win ? "dustin_full_verify_attn_window" : "dustin_full_verify_attn")
+                           : (win ? "dustin_sparse_verify_attn_window"
+                                  : "dustin_sparse_verify_attn");
   int rc = check_attn_shape(b, hq, hkv, d, w, n, what);
   if (rc) return rc;
   if (!dense && (k < 0 || k > n))
@@ -244,6 +265,7 @@ int run_attn(bool dense, int b, int hq, int hkv, int d, int w, int n, int k,
     return fail(DUSTIN_ERR_INVALID_ARG, "%s: unknown flags 0x%x", what, flags);
   rc = check_kv(kv, b, n, d, true, what);
   if (rc) return rc;
+  if (win && (rc = check_win(win, d, what))) return rc;
   const bool paged = kv->page_table != nullptr;
   cudaError_t e;
   if (!dense) {
@@ -274,12 +296,14 @@ int run_attn(bool dense, int b, int hq, int hkv, int d, int w, int n, int k,
     a.chunk = p.chunk;
     a.scale_log2 = scale * kLog2e;
     a.kv_ready = (flags & DUSTIN_ATTN_KV_READY) ? 1 : 0;
+    a.has_win = win ? 1 : 0;
+    if (win) a.win = to_view(*win);
     a.ws_o = need ? static_cast<float*>(ws) : nullptr;
     a.ws_ml = need ? reinterpret_cast<float2*>(static_cast<char*>(ws) + p.ws_o)
                    : nullptr;
     e = launch_attn_sparse(a, d, p.mt, paged, (cudaStream_t)stream);
   } else {
-    const AttnPlan p = plan_dense(b, hq, hkv, d, w, n);
+    const AttnPlan p = plan_dense(b, hq, hkv, d, w, n, win != nullptr);
     const long long T = p.units * p.tpu;
     if (p.units > 0x7fffffffLL || p.grid > 0x7fffffffLL || T > (1LL << 40) ||
         p.grid * T > (1LL << 62) ||
@@ -305,6 +329,9 @@ int run_attn(bool dense, int b, int hq, int hkv, int d, int w, int n, int k,
     a.row_blocks = p.row_blocks;
     a.units = (int)p.units;
     a.tpu = p.tpu;
+    a.tph = p.tph;
+    a.has_win = win ? 1 : 0;
+    if (win) a.win = to_view(*win);
     a.grid = (int)p.grid;
     a.scale_log2 = scale * kLog2e;
     a.kv_ready = (flags & DUSTIN_ATTN_KV_READY) ? 1 : 0;
@@ -500,8 +527,19 @@ int dustin_sparse_verify_attn(int b, int h_q, int h_kv, int d, int w, int n,
                               const int32_t* idx, float scale, void* o,
                               float* lse, void* ws, size_t ws_bytes,
                               unsigned flags, void* stream) {
-  return run_attn(false, b, h_q, h_kv, d, w, n, k, q, kv, idx, scale, o, lse, ws,
-                  ws_bytes, flags, stream);
+  return run_attn(false, b, h_q, h_kv, d, w, n, k, q, kv, idx, nullptr, scale, o,
+                  lse, ws, ws_bytes, flags, stream);
+}
+
+int dustin_sparse_verify_attn_window(int b, int h_q, int h_kv, int d, int w,
+                                     int n, int k, const void* q,
+                                     const dustin_kv* kv, const int32_t* idx,
+                                     const dustin_kv* win, float scale, void* o,
+                                     float* lse, void* ws, size_t ws_bytes,
+                                     unsigned flags, void* stream) {
+  if (!win) return fail(DUSTIN_ERR_INVALID_ARG, "dustin_sparse_verify_attn_window: win is NULL");
+  return run_attn(false, b, h_q, h_kv, d, w, n, k, q, kv, idx, win, scale, o, lse,
+                  ws, ws_bytes, flags, stream);
 }
 
 size_t dustin_full_verify_attn_workspace_size(int b, int h_q, int h_kv, int d,
@@ -509,14 +547,26 @@ size_t dustin_full_verify_attn_workspace_size(int b, int h_q, int h_kv, int d,
   if (b <= 0 || h_q <= 0 || h_kv <= 0 || h_q % h_kv || w <= 0 || n < 0 ||
       (d != 64 && d != 128))
     return 0;
-  return plan_dense(b, h_q, h_kv, d, w, n).workspace();
+  // Covers the call with and without the window merged in.
+  return std::max(plan_dense(b, h_q, h_kv, d, w, n, false).workspace(),
+                  plan_dense(b, h_q, h_kv, d, w, n, true).workspace());
 }
 
 int dustin_full_verify_attn(int b, int h_q, int h_kv, int d, int w, int n,
                             const void* q, const dustin_kv* kv, float scale,
                             void* o, float* lse, void* ws, size_t ws_bytes,
                             unsigned flags, void* stream) {
-  return run_attn(true, b, h_q, h_kv, d, w, n, n, q, kv, nullptr, scale, o, lse,
+  return run_attn(true, b, h_q, h_kv, d, w, n, n, q, kv, nullptr, nullptr, scale, o,
+                  lse, ws, ws_bytes, flags, stream);
+}
+
+int dustin_full_verify_attn_window(int b, int h_q, int h_kv, int d, int w, int n,
+                                   const void* q, const dustin_kv* kv,
+                                   const dustin_kv* win, float scale, void* o,
+                                   float* lse, void* ws, size_t ws_bytes,
+                                   unsigned flags, void* stream) {
+  if (!win) return fail(DUSTIN_ERR_INVALID_ARG, "dustin_full_verify_attn_window: win is NULL");
+  return run_attn(true, b, h_q, h_kv, d, w, n, n, q, kv, nullptr, win, scale, o, lse,
                   ws, ws_bytes, flags, stream);
 }
 

@@ -63,6 +63,8 @@ struct AttnArgs {
   int chunk;        // positions per split (multiple of 64)
   float scale_log2; // scale * log2(e)
   int kv_ready;     // idx, page table and K/V may be read before the wait
+  KvView win;       // the window's own K/V [b][hkv][w][d] (has_win)
+  int has_win;      // merge the window's causal block (last split only)
   float* ws_o;      // [blocks][splits][16 MT][D] (splits > 1)
   float2* ws_ml;    // [blocks][splits][16 MT]    (m in log2 units, l)
 };
@@ -160,7 +162,10 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
   const int p_begin = split * a.chunk;
   const int p_end = min(a.npos, p_begin + a.chunk);
   const int len = max(0, p_end - p_begin);
-  const int ntiles = (len + C::TILE - 1) / C::TILE;
+  const int ntiles = (len + C::TILE - 1) / C::TILE;   // history tiles
+  // With the window merged in, the last split runs one more tile: the w
+  // window rows, causal (row t sees window positions 0..t).
+  const int ntot = ntiles + ((a.has_win && split == a.splits - 1) ? 1 : 0);
 
   const long long unit_off = (long long)bb * a.kv.sb + (long long)g * a.kv.sh;
   // The kv heads of a sequence share one index set, so their CTAs would
@@ -256,24 +261,36 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
       return i < len ? tab[i] : -1;
     };
 
-    // kv_ready: the first n_pre tiles go out before this thread's wait.
-    const int n_pre = a.kv_ready ? min(ntiles, C::STAGES) : -1;
-    if (n_pre == 0) {
-      griddep_wait();
-      griddep_launch_dependents();
-    }
-    for (int t = 0; t < ntiles; ++t) {
-      const int s = t % C::STAGES;
-      if (t == n_pre) {
-        griddep_wait();
-        griddep_launch_dependents();
+    // kv_ready: the first n_pre history tiles go out before this thread's
+    // wait (the window tile, like q, is read only after it).
+    const int n_pre = a.kv_ready ? min(ntiles, C::STAGES) : 0;
+    bool waited = false;
+    auto ensure_wait = [&]() {
+      if (!waited) {
+        if (a.kv_ready) {
+          griddep_wait();
+          griddep_launch_dependents();
+        }
+        waited = true;
       }
+    };
+    for (int t = 0; t < ntot; ++t) {
+      const int s = t % C::STAGES;
+      if (t >= n_pre) ensure_wait();
       if (t >= C::STAGES &&
           !mbar_wait(empty_bar(s), ((t / C::STAGES) & 1) ^ 1, kWaitLimitCycles)) {
         if (lane == 0) atomicOr(&g_attn_dev_flags, 4u);
         break;
       }
-      const long long my_off = row_offset(tile_of(t), my_row);
+      const bool wtile = t == ntiles;
+      long long my_off;
+      if (!wtile)
+        my_off = row_offset(tile_of(t), my_row);
+      else
+        my_off = my_row < a.w ? (long long)bb * a.win.sb + (long long)g * a.win.sh +
+                                    (long long)my_row * a.win.sn
+                              : -1;
+      const __nv_bfloat16* src = wtile ? (is_v ? a.win.v : a.win.k) : src_base;
       const unsigned vm = __ballot_sync(0xffffffffu, my_off >= 0) &
                           (C::RPW == 32 ? 0xffffffffu : ((1u << C::RPW) - 1u));
       unsigned char* dst = dst_base + s * C::TILE_BYTES + ch * 16;
@@ -284,12 +301,12 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
         const uint32_t d = smem_u32(dst + (pw * C::RPW + rr) * C::RS);
 #if DUSTIN_ATTN_PLAIN_CP
         if (off >= 0)
-          cp_async_16_full(d, src_base + off + ch * 8);
+          cp_async_16_full(d, src + off + ch * 8);
         else
-          cp_async_16(d, src_base, 0);            // zero-fill a left-out row
+          cp_async_16(d, src, 0);                 // zero-fill a left-out row
 #else
         const bool ok = off >= 0;
-        cp_async_16(d, src_base + (ok ? off + ch * 8 : 0), ok ? 16 : 0);
+        cp_async_16(d, src + (ok ? off + ch * 8 : 0), ok ? 16 : 0);
 #endif
       }
       cp_async_mbar_arrive(full_bar(s));
@@ -303,10 +320,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
         mbar_arrive(full_bar(s));
       }
     }
-    if (n_pre == ntiles && ntiles > 0) {   // every tile went out early
-      griddep_wait();
-      griddep_launch_dependents();
-    }
+    ensure_wait();
     // Every copy of this thread lands before the CTA may exit.
     cp_async_wait<0>();
     return;
@@ -342,7 +356,9 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   const int gq = lane >> 2, tq = lane & 3;
 
-  for (int t = 0; t < ntiles; ++t) {
+  // Window position of rows 16 wm + gq and + 8 (rows past G*w: unused).
+  const int tA = (r_lo + wm * 16 + gq) % a.w, tB = (r_lo + wm * 16 + gq + 8) % a.w;
+  for (int t = 0; t < ntot; ++t) {
     const int s = t % C::STAGES;
     if (!mbar_wait(full_bar(s), (t / C::STAGES) & 1, kWaitLimitCycles)) {
       if (lane == 0) atomicOr(&g_attn_dev_flags, 4u);
@@ -394,7 +410,16 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
     // Rows left out of the tile get -inf.  Scores stay unscaled here: the
     // scale (> 0) is folded into the exponent below, so the maximum is taken
     // on raw scores and converted once per row.
-    if (vmask != ~0ull) {
+    if (t == ntiles) {   // the window tile: causal within the window
+#pragma unroll
+      for (int j = 0; j < C::NT8; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int pos = wn * C::PW + j * 8 + 2 * tq + e;
+          sc[j][e] = pos <= tA ? sc[j][e] : -INFINITY;
+          sc[j][e + 2] = pos <= tB ? sc[j][e + 2] : -INFINITY;
+        }
+    } else if (vmask != ~0ull) {
 #pragma unroll
       for (int j = 0; j < C::NT8; ++j)
 #pragma unroll

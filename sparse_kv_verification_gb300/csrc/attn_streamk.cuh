@@ -55,10 +55,13 @@ struct AttnSkArgs {
   int rows;         // group * w
   int row_blocks;   // ceil(rows / (16 * MT))
   int units;        // b * hkv * row_blocks
-  int tpu;          // tiles per unit: max(1, ceil(n / 64))
+  int tph;          // history tiles per unit: ceil(n / 64)
+  int tpu;          // tiles per unit: max(1, tph + has_win)
   int grid;         // CTAs (G)
   float scale_log2; // scale * log2(e)
   int kv_ready;     // the page table and K/V may be read before the wait
+  KvView win;       // the window's own K/V [b][hkv][w][d] (has_win)
+  int has_win;      // a unit's last tile is its window tile (causal)
   float* ws_o;      // [2 G][16 MT][D] partial O   (when some unit is split)
   float2* ws_ml;    // [2 G][16 MT] (m in log2 units, l)
   unsigned long long* counters;  // [units] (epoch << 24 | count)
@@ -192,11 +195,12 @@ __global__ void __launch_bounds__(SkCfg<D, MT>::NT, 1)
   // share its index set, so without a rotation the CTAs of one sequence
   // would read the same positions of eight K/V slabs a power of two apart
   // at the same moments; starting head g at tile g tpu / hkv spreads them.
+  // (History tiles only: lt < tph.)
   auto phys_tile = [&](int lt, int g) {
     if (!DUSTIN_ATTN_ROTATE) return lt;
-    const long long gt = (long long)g * a.tpu;
+    const long long gt = (long long)g * a.tph;
     const int t = lt + (gt <= 0x7fffffffLL ? (int)gt / a.hkv : (int)(gt / a.hkv));
-    return t >= a.tpu ? t - a.tpu : t;
+    return t >= a.tph ? t - a.tph : t;
   };
   // Unit u and local tile range [lt0, lt1) of segment s.
   // (Reads the range back from shared memory, so that the pipelines do not
@@ -262,7 +266,9 @@ __global__ void __launch_bounds__(SkCfg<D, MT>::NT, 1)
         const int x = lt_first + tt;
         const int ug = (u0 + x / a.tpu) / a.row_blocks;
         const int g = ug % a.hkv;
-        tinfo[tt] = make_int4(ug / a.hkv, g, phys_tile(x % a.tpu, g) * C::TILE, 0);
+        const int lt = x % a.tpu;   // the window tile has no page entries
+        tinfo[tt] = make_int4(ug / a.hkv, g,
+                              lt < a.tph ? phys_tile(lt, g) * C::TILE : -(1 << 30), 0);
       }
     }
     __syncthreads();
@@ -275,7 +281,7 @@ __global__ void __launch_bounds__(SkCfg<D, MT>::NT, 1)
       if (i < n_ent) {
         const int4 ti = tinfo[i / PER_TILE];
         const int p = ti.z + (i % PER_TILE) * 16;
-        if (p < a.n)
+        if (p >= 0 && p < a.n)
           key[r] = __ldg(a.kv.page_table + (long long)ti.x * a.kv.pages_per_seq +
                          p / a.kv.page_size);
       }
@@ -287,7 +293,7 @@ __global__ void __launch_bounds__(SkCfg<D, MT>::NT, 1)
       const int4 ti = tinfo[i / PER_TILE];
       const int p = ti.z + (i % PER_TILE) * 16;
       long long off = -1;
-      if (p < a.n) {
+      if (p >= 0 && p < a.n) {
         const int pg = key[r];
         if (pg < 0 || pg >= a.kv.num_pages)
           atomicOr(&g_attn_sk_dev_flags, 2u);
@@ -333,9 +339,12 @@ __global__ void __launch_bounds__(SkCfg<D, MT>::NT, 1)
     for (int s = 0; s < nseg && ok_run; ++s) {
       int u, lt0, lt1;
       seg_range(s, u, lt0, lt1);
-      const int rot = phys_tile(0, (u / a.row_blocks) % a.hkv);
+      const int ug = u / a.row_blocks;
+      const int rot = a.tph > 0 ? phys_tile(0, ug % a.hkv) : 0;
       long long kv_off = 0;
       if constexpr (!PAGED) kv_off = unit_of(u).kv_off;
+      const long long win_off =
+          (long long)(ug / a.hkv) * a.win.sb + (long long)(ug % a.hkv) * a.win.sh;
       if (s > 0) {
         ensure_wait();
         // The consumers took the previous query rows into registers.
@@ -356,17 +365,24 @@ __global__ void __launch_bounds__(SkCfg<D, MT>::NT, 1)
           break;
         }
         long long my_off = -1;
-        int pt = lt + rot;
-        pt = pt >= a.tpu ? pt - a.tpu : pt;
-        const int p = pt * C::TILE + my_row;  // position in the unit
-        if (p < a.n) {
-          if constexpr (PAGED) {
-            const long long base = tab[t * (C::TILE / 16) + my_row / 16];
-            my_off = base < 0 ? -1 : base + (long long)(my_row % 16) * a.kv.sn;
-          } else {
-            my_off = kv_off + (long long)p * a.kv.sn;
+        const bool wtile = a.has_win && lt == a.tph;
+        if (wtile) {   // the window rows, read (like q) only after the wait
+          ensure_wait();
+          if (my_row < a.w) my_off = win_off + (long long)my_row * a.win.sn;
+        } else {
+          int pt = lt + rot;
+          pt = pt >= a.tph ? pt - a.tph : pt;
+          const int p = pt * C::TILE + my_row;  // position in the unit
+          if (p < a.n) {
+            if constexpr (PAGED) {
+              const long long base = tab[t * (C::TILE / 16) + my_row / 16];
+              my_off = base < 0 ? -1 : base + (long long)(my_row % 16) * a.kv.sn;
+            } else {
+              my_off = kv_off + (long long)p * a.kv.sn;
+            }
           }
         }
+        const __nv_bfloat16* src = wtile ? (is_v ? a.win.v : a.win.k) : src_base;
         const unsigned vm = __ballot_sync(0xffffffffu, my_off >= 0) &
                             (C::RPW == 32 ? 0xffffffffu : ((1u << C::RPW) - 1u));
         unsigned char* dst = dst_base + st * C::TILE_BYTES + ch * 16;
@@ -376,7 +392,7 @@ __global__ void __launch_bounds__(SkCfg<D, MT>::NT, 1)
           const long long off = __shfl_sync(0xffffffffu, my_off, rr);
           const bool ok = off >= 0;
           cp_async_16(smem_u32(dst + (pw * C::RPW + rr) * C::RS),
-                      src_base + (ok ? off + ch * 8 : 0), ok ? 16 : 0);
+                      src + (ok ? off + ch * 8 : 0), ok ? 16 : 0);
         }
         cp_async_mbar_arrive(full_bar(st));
         if (lane == 0) {
@@ -421,11 +437,17 @@ __global__ void __launch_bounds__(SkCfg<D, MT>::NT, 1)
   };
 
   for (int sgi = 0; sgi < nseg; ++sgi) {
-    int seg_tiles;
+    int seg_tiles, seg_lt0, tA = 0, tB = 0;
     {
       int u, lt0, lt1;
       seg_range(sgi, u, lt0, lt1);
       seg_tiles = lt1 - lt0;
+      seg_lt0 = lt0;
+      if (a.has_win) {   // window position of rows 16 wm + gq and + 8
+        const int r0 = (u % a.row_blocks) * C::ROWS + wm * 16 + gq;
+        tA = r0 % a.w;
+        tB = (r0 + 8) % a.w;
+      }
     }
     if (sgi > 0) wait_or_die(q_full, (sgi - 1) & 1);
     uint32_t qf[C::KS][4];
@@ -495,7 +517,16 @@ __global__ void __launch_bounds__(SkCfg<D, MT>::NT, 1)
       // Rows left out of the tile get -inf.  Scores stay unscaled here: the
       // scale (> 0) is folded into the exponent below, so the maximum is
       // taken on raw scores and converted once per row.
-      if (vmask != ~0ull) {
+      if (a.has_win && seg_lt0 + i == a.tph) {   // the window: causal
+#pragma unroll
+        for (int j = 0; j < C::NT8; ++j)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int pos = wn * C::PW + j * 8 + 2 * tq + e;
+            sc[j][e] = pos <= tA ? sc[j][e] : -INFINITY;
+            sc[j][e + 2] = pos <= tB ? sc[j][e + 2] : -INFINITY;
+          }
+      } else if (vmask != ~0ull) {
 #pragma unroll
         for (int j = 0; j < C::NT8; ++j)
 #pragma unroll

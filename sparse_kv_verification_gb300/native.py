@@ -27,7 +27,9 @@ EXPORTS = (
     "dustin_score_heads_noalloc",
     "dustin_hybrid_topk",
     "dustin_sparse_verify_attn_workspace_size", "dustin_sparse_verify_attn",
+    "dustin_sparse_verify_attn_window",
     "dustin_full_verify_attn_workspace_size", "dustin_full_verify_attn",
+    "dustin_full_verify_attn_window",
 )
 
 
@@ -92,6 +94,10 @@ def load(build_if_missing: bool = False, path: Optional[str] = None
         "dustin_full_verify_attn_workspace_size": (S, [I, I, I, I, I, I]),
         "dustin_full_verify_attn": (I, [I, I, I, I, I, I, P, P, F, P, P, P, S,
                                         U, P]),
+        "dustin_sparse_verify_attn_window": (I, [I, I, I, I, I, I, I, P, P, P, P,
+                                                 F, P, P, P, S, U, P]),
+        "dustin_full_verify_attn_window": (I, [I, I, I, I, I, I, P, P, P, F, P, P,
+                                               P, S, U, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -281,6 +287,39 @@ def dustin_full_verify_attn(q: torch.Tensor, kv: DustinKV, h_kv: int, n: int,
         b, h_q, h_kv, d, w, n, q.data_ptr(), ctypes.byref(kv), float(scale),
         o.data_ptr(), lse.data_ptr(), _ptr(ws), 0 if ws is None else ws.numel(),
         int(flags), _stream(stream, q.device)))
+
+
+def dustin_sparse_verify_attn_window(q: torch.Tensor, kv: DustinKV, h_kv: int,
+                                     n: int, idx: torch.Tensor, win: DustinKV,
+                                     scale: float, o: torch.Tensor,
+                                     lse: torch.Tensor,
+                                     ws: Optional[torch.Tensor], stream=None,
+                                     flags: int = 0) -> None:
+    """dustin_sparse_verify_attn with the window's causal block merged in;
+    win describes the window tokens' K/V [b][h_kv][w][d] (kv_desc)."""
+    _attn_checks(q, o, lse)
+    b, h_q, w, d = q.shape
+    if idx.dtype != torch.int32 or not idx.is_contiguous() or idx.dim() != 2 \
+            or idx.shape[0] != b:
+        raise ValueError("idx must be contiguous int32 [b][k]")
+    _check(load().dustin_sparse_verify_attn_window(
+        b, h_q, h_kv, d, w, n, idx.shape[1], q.data_ptr(), ctypes.byref(kv),
+        idx.data_ptr(), ctypes.byref(win), float(scale), o.data_ptr(),
+        lse.data_ptr(), _ptr(ws), 0 if ws is None else ws.numel(), int(flags),
+        _stream(stream, q.device)))
+
+
+def dustin_full_verify_attn_window(q: torch.Tensor, kv: DustinKV, h_kv: int,
+                                   n: int, win: DustinKV, scale: float,
+                                   o: torch.Tensor, lse: torch.Tensor,
+                                   ws: Optional[torch.Tensor], stream=None,
+                                   flags: int = 0) -> None:
+    _attn_checks(q, o, lse)
+    b, h_q, w, d = q.shape
+    _check(load().dustin_full_verify_attn_window(
+        b, h_q, h_kv, d, w, n, q.data_ptr(), ctypes.byref(kv), ctypes.byref(win),
+        float(scale), o.data_ptr(), lse.data_ptr(), _ptr(ws),
+        0 if ws is None else ws.numel(), int(flags), _stream(stream, q.device)))
 
 
 # ------------------------------------------------------------------ misc

@@ -48,6 +48,37 @@ def full_attn(q, k, v, scale, n=None, page_table=None):
     return o, lse
 
 
+def sparse_attn_window(q, k, v, idx, kw, vw, scale, n=None, page_table=None,
+                       flags=0):
+    b, hq, w, d = q.shape
+    hkv = k.shape[1]
+    n = k.shape[2] if n is None else n
+    ws = N.workspace(N.dustin_sparse_verify_attn_workspace_size(
+        b, hq, hkv, d, w, idx.shape[1]), q.device)
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((b, hq, w), float("nan"), device=q.device)
+    N.dustin_sparse_verify_attn_window(q, N.kv_desc(k, v, page_table), hkv, n,
+                                       idx, N.kv_desc(kw, vw), scale, o, lse, ws,
+                                       flags=flags)
+    sync()
+    return o, lse
+
+
+def full_attn_window(q, k, v, kw, vw, scale, n=None, page_table=None, flags=0):
+    b, hq, w, d = q.shape
+    hkv = k.shape[1]
+    n = k.shape[2] if n is None else n
+    ws = N.workspace(N.dustin_full_verify_attn_workspace_size(
+        b, hq, hkv, d, w, n), q.device)
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((b, hq, w), float("nan"), device=q.device)
+    N.dustin_full_verify_attn_window(q, N.kv_desc(k, v, page_table), hkv, n,
+                                     N.kv_desc(kw, vw), scale, o, lse, ws,
+                                     flags=flags)
+    sync()
+    return o, lse
+
+
 def score(q, keys, kv_heads, scale, n, page_tables=None):
     """q [P][b][rows][d]; keys: list of K tensors (one per pair)."""
     p, b, rows, d = q.shape

@@ -153,6 +153,62 @@ def test_kv_ready_launch_overlap_gives_identical_results(case):
         assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+# ------------------------------------------- window causal block merged in
+
+WINDOW_SHAPES = [SHAPES[0], SHAPES[2], SHAPES[4], SHAPES[6], SHAPES[9],
+                 (2, 16, 2, 128, 4, 40, 0)]
+
+
+@pytest.mark.parametrize("shape", WINDOW_SHAPES, ids=[str(s) for s in WINDOW_SHAPES])
+def test_window_attention_parity(shape):
+    """History over idx (sparse) or all n (dense) plus the window's own
+    causal block, in one launch, against the oracle.  Covers several row
+    blocks, position splits, the dense stream-K ranges and k = 0."""
+    b, hq, hkv, d, w, n, k = shape
+    q, kk, v = qkv(b, hq, hkv, d, w, n, seed=sum(shape) + 7)
+    _, kw, vw = qkv(b, hq, hkv, d, w, w, seed=sum(shape) + 8)
+    idx = I.random_sorted_indices(b, n, k, seed=k + n + 1) if k else \
+        torch.zeros((b, 0), dtype=torch.int32)
+    dq, dk, dv, dkw, dvw = (t.to(DEV) for t in (q, kk, v, kw, vw))
+    scale = d ** -0.5
+    o, lse = H.sparse_attn_window(dq, dk, dv, idx.to(DEV), dkw, dvw, scale)
+    o_ref, l_ref = O.verify_attention_window(H.f64(q), H.f64(kk), H.f64(v),
+                                             idx.numpy(), H.f64(kw), H.f64(vw),
+                                             scale)
+    H.assert_attn_close(o, lse, o_ref, l_ref)
+    if k:   # the dense call (k = 0 is a sparse-only case)
+        o, lse = H.full_attn_window(dq, dk, dv, dkw, dvw, scale)
+        o_ref, l_ref = O.verify_attention_window(H.f64(q), H.f64(kk), H.f64(v),
+                                                 None, H.f64(kw), H.f64(vw),
+                                                 scale)
+        H.assert_attn_close(o, lse, o_ref, l_ref)
+    assert N.dustin_device_status() == 0
+
+
+def test_window_attention_paged_and_kv_ready():
+    b, hq, hkv, d, w, n, k = 2, 16, 2, 128, 4, 1000, 300
+    q, kk, v = qkv(b, hq, hkv, d, w, n, seed=31)
+    _, kw, vw = qkv(b, hq, hkv, d, w, w, seed=32)
+    pk, pv, table = I.to_paged(kk, v, 16, seed=33)
+    idx = I.random_sorted_indices(b, n, k, seed=34).to(DEV)
+    dq, dkw, dvw = q.to(DEV), kw.to(DEV), vw.to(DEV)
+    o_c, l_c = H.sparse_attn_window(dq, kk.to(DEV), v.to(DEV), idx, dkw, dvw, 0.1)
+    o_p, l_p = H.sparse_attn_window(dq, pk.to(DEV), pv.to(DEV), idx, dkw, dvw, 0.1,
+                                    n=n, page_table=table.to(DEV),
+                                    flags=N.DUSTIN_ATTN_KV_READY)
+    assert torch.equal(o_c, o_p) and torch.equal(l_c, l_p)
+    f_c, fl_c = H.full_attn_window(dq, kk.to(DEV), v.to(DEV), dkw, dvw, 0.1)
+    f_p, fl_p = H.full_attn_window(dq, pk.to(DEV), pv.to(DEV), dkw, dvw, 0.1, n=n,
+                                   page_table=table.to(DEV),
+                                   flags=N.DUSTIN_ATTN_KV_READY)
+    assert torch.equal(f_c, f_p) and torch.equal(fl_c, fl_p)
+    o_ref, l_ref = O.verify_attention_window(H.f64(q), H.f64(kk), H.f64(v),
+                                             idx.cpu().numpy(), H.f64(kw),
+                                             H.f64(vw), 0.1)
+    H.assert_attn_close(o_p, l_p, o_ref, l_ref)
+    assert N.dustin_device_status() == 0
+
+
 def test_sparse_with_all_positions_matches_full():
     b, hq, hkv, d, w, n = 2, 16, 2, 128, 4, 777
     q, kk, v = qkv(b, hq, hkv, d, w, n, seed=5)

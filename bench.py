@@ -59,6 +59,8 @@ def parse_args(argv=None):
     p.add_argument("--no-dense", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--no-extras", action="store_true",
+                   help="skip the window-merge and naive-estimator numbers")
     p.add_argument("--cpu-rows", type=int, default=1)
     p.add_argument("--cpu-layers", type=int, default=2)
     p.add_argument("--cpu-reps", type=int, default=2)
@@ -265,6 +267,72 @@ class Replica:
     def bytes_select(self):
         wl = self.wl
         return 2 * wl.b * wl.n * 4 + wl.b * min(wl.k, wl.n) * 4
+
+
+# ----------------------------------------------------------------- extras
+
+def run_extras(rep, wl, dev, stream, L, args, t_attn, t_dense):
+    """Per-layer times of the window-merge entry points (the w x w causal
+    block as one more tile of the same launch), and one step of the naive
+    estimator: every target query head of every layer scored."""
+    import torch
+    from sparse_kv_verification_gb300 import native as N
+    inp = rep.inp
+    g = torch.Generator(device=dev)
+    g.manual_seed(4321)
+    shape = (wl.b, wl.hkv, wl.w, wl.d)
+    wins = [(torch.randn(shape, generator=g, device=dev).to(torch.bfloat16),
+             torch.randn(shape, generator=g, device=dev).to(torch.bfloat16))
+            for _ in range(L)]
+    kv = [N.kv_desc(k, v) for k, v in zip(inp.k, inp.v)]
+    ready = lambda l: N.DUSTIN_ATTN_KV_READY if l > 0 else 0
+    sw = [N.prepare_sparse_verify_attn_window(
+        inp.q[l], kv[l], wl.hkv, wl.n, rep.idx, N.kv_desc(*wins[l]), wl.scale,
+        rep.o[l], rep.lse[l], rep.ws_a, flags=ready(l)) for l in range(L)]
+    fw = [N.prepare_full_verify_attn_window(
+        inp.q[l], kv[l], wl.hkv, wl.n, N.kv_desc(*wins[l]), wl.scale, rep.o[l],
+        rep.lse[l], rep.ws_f, flags=ready(l)) for l in range(L)]
+
+    def time_pass(calls, reps):
+        for c in calls:
+            c()
+        torch.cuda.synchronize(dev)
+        e0, e1 = (torch.cuda.Event(enable_timing=True),
+                  torch.cuda.Event(enable_timing=True))
+        e0.record(stream)
+        for _ in range(reps):
+            for c in calls:
+                c()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) * 1e3 / (reps * len(calls))
+
+    t_sw = time_pass(sw, 5)
+    t_fw = time_pass(fw, 1) if not args.no_dense else None
+    # Naive estimator: all h_q heads of each layer as that layer's scored
+    # pairs (latest-token query, one row), one scoring call per layer.
+    hq = wl.hq
+    q_all = torch.randn((hq, wl.b, 1, wl.d), generator=g, device=dev).to(torch.bfloat16)
+    s_out = torch.empty((wl.b, wl.n), device=dev)
+    ws = N.workspace(N.dustin_score_heads_workspace_size(wl.b, wl.n, hq, 1), dev)
+    heads = [h // wl.group for h in range(hq)]
+    naive = [N.prepare_score_heads(q_all, [N.kv_desc(inp.k[l])] * hq, heads,
+                                   wl.scale, s_out, ws, wl.n) for l in range(L)]
+    t_naive_layer = time_pass(naive, 1)
+    return {
+        "window_sparse_us_per_layer": t_sw,
+        "window_sparse_overhead_us": t_sw - t_attn,
+        "window_dense_us_per_layer": t_fw,
+        "window_dense_overhead_us": (t_fw - t_dense) if (t_fw and t_dense) else None,
+        "naive_estimator": {
+            "what": (f"all {hq} target query heads of each of {L} layers scored "
+                     "(latest-token query), one scoring call per layer; draft "
+                     "side not included"),
+            "ms_per_step": t_naive_layer * L / 1e3,
+            "dense_attention_ms_per_step": (t_dense * L / 1e3) if t_dense else None,
+            "ratio_to_dense": (t_naive_layer / t_dense) if t_dense else None,
+        },
+    }
 
 
 # ----------------------------------------------------------------- oracle leg
@@ -553,6 +621,13 @@ def run_ours(args):
                "unit": UNIT, "ms_per_step": t_e2e,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
+    # ---- extras: the window's causal block merged in (sparse and dense),
+    # and the naive estimator (every target head of every layer scored).
+    extras = None
+    if not args.no_extras:
+        extras = run_extras(rep, wl, dev, stream, L, args, t_attn,
+                            dense["us_per_layer"] if dense else None)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         res = run_oracle_leg(args, args.cpu_reps, 1)
@@ -583,6 +658,7 @@ def run_ours(args):
                      "traffic": committed_traffic()},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
         "clocks": clock_info, "kernels": kernels, "dense": dense,
+        "extras": extras,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -64,7 +64,8 @@ struct AttnArgs {
   float scale_log2; // scale * log2(e)
   int kv_ready;     // idx, page table and K/V may be read before the wait
   KvView win;       // the window's own K/V [b][hkv][w][d] (has_win)
-  int has_win;      // merge the window's causal block (last split only)
+  int has_win;      // merge the window's causal block (last split only;
+                    // selects the WIN instance of the kernel)
   float* ws_o;      // [blocks][splits][16 MT][D] (splits > 1)
   float2* ws_ml;    // [blocks][splits][16 MT]    (m in log2 units, l)
 };
@@ -131,7 +132,7 @@ struct AttnCfg {
 static __device__ unsigned int g_attn_dev_flags;
 
 
-template <int D, int MT, bool PAGED>
+template <int D, int MT, bool PAGED, bool WIN>
 __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
     verify_attn_kernel(const AttnArgs a) {
   using C = AttnCfg<D, MT>;
@@ -165,7 +166,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
   const int ntiles = (len + C::TILE - 1) / C::TILE;   // history tiles
   // With the window merged in, the last split runs one more tile: the w
   // window rows, causal (row t sees window positions 0..t).
-  const int ntot = ntiles + ((a.has_win && split == a.splits - 1) ? 1 : 0);
+  const int ntot = ntiles + ((WIN && split == a.splits - 1) ? 1 : 0);
 
   const long long unit_off = (long long)bb * a.kv.sb + (long long)g * a.kv.sh;
   // The kv heads of a sequence share one index set, so their CTAs would
@@ -263,26 +264,19 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
 
     // kv_ready: the first n_pre history tiles go out before this thread's
     // wait (the window tile, like q, is read only after it).
-    const int n_pre = a.kv_ready ? min(ntiles, C::STAGES) : 0;
-    bool waited = false;
-    auto ensure_wait = [&]() {
-      if (!waited) {
-        if (a.kv_ready) {
-          griddep_wait();
-          griddep_launch_dependents();
-        }
-        waited = true;
-      }
-    };
+    const int n_pre = a.kv_ready ? min(ntiles, C::STAGES) : -1;
     for (int t = 0; t < ntot; ++t) {
       const int s = t % C::STAGES;
-      if (t >= n_pre) ensure_wait();
+      if (t == n_pre) {
+        griddep_wait();
+        griddep_launch_dependents();
+      }
       if (t >= C::STAGES &&
           !mbar_wait(empty_bar(s), ((t / C::STAGES) & 1) ^ 1, kWaitLimitCycles)) {
         if (lane == 0) atomicOr(&g_attn_dev_flags, 4u);
         break;
       }
-      const bool wtile = t == ntiles;
+      const bool wtile = WIN && t == ntiles;
       long long my_off;
       if (!wtile)
         my_off = row_offset(tile_of(t), my_row);
@@ -320,7 +314,10 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
         mbar_arrive(full_bar(s));
       }
     }
-    ensure_wait();
+    if (n_pre >= ntot) {   // kv_ready, and every tile went out early
+      griddep_wait();
+      griddep_launch_dependents();
+    }
     // Every copy of this thread lands before the CTA may exit.
     cp_async_wait<0>();
     return;
@@ -357,7 +354,8 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
   const int gq = lane >> 2, tq = lane & 3;
 
   // Window position of rows 16 wm + gq and + 8 (rows past G*w: unused).
-  const int tA = (r_lo + wm * 16 + gq) % a.w, tB = (r_lo + wm * 16 + gq + 8) % a.w;
+  const int tA = WIN ? (r_lo + wm * 16 + gq) % a.w : 0;
+  const int tB = WIN ? (r_lo + wm * 16 + gq + 8) % a.w : 0;
   for (int t = 0; t < ntot; ++t) {
     const int s = t % C::STAGES;
     if (!mbar_wait(full_bar(s), (t / C::STAGES) & 1, kWaitLimitCycles)) {
@@ -410,7 +408,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
     // Rows left out of the tile get -inf.  Scores stay unscaled here: the
     // scale (> 0) is folded into the exponent below, so the maximum is taken
     // on raw scores and converted once per row.
-    if (t == ntiles) {   // the window tile: causal within the window
+    if (WIN && t == ntiles) {   // the window tile: causal within the window
 #pragma unroll
       for (int j = 0; j < C::NT8; ++j)
 #pragma unroll

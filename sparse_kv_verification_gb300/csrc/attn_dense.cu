@@ -7,7 +7,7 @@
 namespace dustin {
 namespace {
 
-template <int D, int MT, bool PAGED>
+template <int D, int MT, bool PAGED, bool WIN>
 cudaError_t prepare() {
   using C = SkCfg<D, MT>;
   static std::atomic<uint64_t> done{0};
@@ -18,7 +18,7 @@ cudaError_t prepare() {
     static std::atomic<int> checked{0};
     if (checked.load() == 0) {
       cudaFuncAttributes fa;
-      cudaError_t e = cudaFuncGetAttributes(&fa, verify_attn_sk_kernel<D, MT, PAGED>);
+      cudaError_t e = cudaFuncGetAttributes(&fa, verify_attn_sk_kernel<D, MT, PAGED, WIN>);
       if (e != cudaSuccess) return e;
       const long long have = (long long)fa.numRegs * C::NT;
       const long long need = (long long)C::PRODUCER_REGS * C::NPW * 32 +
@@ -27,36 +27,41 @@ cudaError_t prepare() {
     }
     if (checked.load() < 0) return cudaErrorInvalidConfiguration;
   }
-  return ensure_smem_attr(verify_attn_sk_kernel<D, MT, PAGED>, C::SMEM, done);
+  return ensure_smem_attr(verify_attn_sk_kernel<D, MT, PAGED, WIN>, C::SMEM, done);
 }
 
-template <int D, int MT, bool PAGED>
+template <int D, int MT, bool PAGED, bool WIN>
 cudaError_t run(const AttnSkArgs& a, cudaStream_t st) {
   using C = SkCfg<D, MT>;
-  cudaError_t e = prepare<D, MT, PAGED>();
+  cudaError_t e = prepare<D, MT, PAGED, WIN>();
   if (e != cudaSuccess) return e;
-  e = launch_pdl(verify_attn_sk_kernel<D, MT, PAGED>, dim3((unsigned)a.grid),
+  e = launch_pdl(verify_attn_sk_kernel<D, MT, PAGED, WIN>, dim3((unsigned)a.grid),
                  dim3(C::NT), C::SMEM, st, a);
   if (e == cudaSuccess) note_launches(1);
   return e;
 }
 
-template <int D, bool PAGED>
+template <int D, bool PAGED, bool WIN>
 cudaError_t by_mt(const AttnSkArgs& a, int mt, cudaStream_t st) {
   switch (mt) {
-    case 1: return run<D, 1, PAGED>(a, st);
-    case 2: return run<D, 2, PAGED>(a, st);
-    case 3: return run<D, 3, PAGED>(a, st);
-    default: return run<D, 4, PAGED>(a, st);
+    case 1: return run<D, 1, PAGED, WIN>(a, st);
+    case 2: return run<D, 2, PAGED, WIN>(a, st);
+    case 3: return run<D, 3, PAGED, WIN>(a, st);
+    default: return run<D, 4, PAGED, WIN>(a, st);
   }
+}
+
+template <int D, bool PAGED>
+cudaError_t by_win(const AttnSkArgs& a, int mt, cudaStream_t st) {
+  return a.has_win ? by_mt<D, PAGED, true>(a, mt, st) : by_mt<D, PAGED, false>(a, mt, st);
 }
 
 template <int D, int MT>
 int occ() {
-  if (prepare<D, MT, false>() != cudaSuccess) return 1;
+  if (prepare<D, MT, false, false>() != cudaSuccess) return 1;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-          &n, verify_attn_sk_kernel<D, MT, false>, SkCfg<D, MT>::NT,
+          &n, verify_attn_sk_kernel<D, MT, false, false>, SkCfg<D, MT>::NT,
           SkCfg<D, MT>::SMEM) != cudaSuccess)
     return 1;
   return n > 0 ? n : 1;
@@ -66,8 +71,8 @@ int occ() {
 
 cudaError_t launch_attn_dense(const AttnSkArgs& a, int d, int mt, bool paged,
                               cudaStream_t st) {
-  if (d == 64) return paged ? by_mt<64, true>(a, mt, st) : by_mt<64, false>(a, mt, st);
-  return paged ? by_mt<128, true>(a, mt, st) : by_mt<128, false>(a, mt, st);
+  if (d == 64) return paged ? by_win<64, true>(a, mt, st) : by_win<64, false>(a, mt, st);
+  return paged ? by_win<128, true>(a, mt, st) : by_win<128, false>(a, mt, st);
 }
 
 int occupancy_attn_dense(int d, int mt) {

@@ -61,7 +61,8 @@ struct AttnSkArgs {
   float scale_log2; // scale * log2(e)
   int kv_ready;     // the page table and K/V may be read before the wait
   KvView win;       // the window's own K/V [b][hkv][w][d] (has_win)
-  int has_win;      // a unit's last tile is its window tile (causal)
+  int has_win;      // a unit's last tile is its window tile (causal;
+                    // selects the WIN instance of the kernel)
   float* ws_o;      // [2 G][16 MT][D] partial O   (when some unit is split)
   float2* ws_ml;    // [2 G][16 MT] (m in log2 units, l)
   unsigned long long* counters;  // [units] (epoch << 24 | count)
@@ -146,7 +147,7 @@ __host__ __device__ inline int sk_owner(long long x, long long T, long long G) {
   return (int)(((x + 1) * G - 1) / T);
 }
 
-template <int D, int MT, bool PAGED>
+template <int D, int MT, bool PAGED, bool WIN>
 __global__ void __launch_bounds__(SkCfg<D, MT>::NT, 1)
     verify_attn_sk_kernel(const AttnSkArgs a) {
   using C = SkCfg<D, MT>;
@@ -340,11 +341,12 @@ __global__ void __launch_bounds__(SkCfg<D, MT>::NT, 1)
       int u, lt0, lt1;
       seg_range(s, u, lt0, lt1);
       const int ug = u / a.row_blocks;
-      const int rot = a.tph > 0 ? phys_tile(0, ug % a.hkv) : 0;
+      const int rot = (!WIN || a.tph > 0) ? phys_tile(0, ug % a.hkv) : 0;
       long long kv_off = 0;
       if constexpr (!PAGED) kv_off = unit_of(u).kv_off;
-      const long long win_off =
-          (long long)(ug / a.hkv) * a.win.sb + (long long)(ug % a.hkv) * a.win.sh;
+      long long win_off = 0;
+      if constexpr (WIN)
+        win_off = (long long)(ug / a.hkv) * a.win.sb + (long long)(ug % a.hkv) * a.win.sh;
       if (s > 0) {
         ensure_wait();
         // The consumers took the previous query rows into registers.
@@ -365,7 +367,7 @@ __global__ void __launch_bounds__(SkCfg<D, MT>::NT, 1)
           break;
         }
         long long my_off = -1;
-        const bool wtile = a.has_win && lt == a.tph;
+        const bool wtile = WIN && lt == a.tph;
         if (wtile) {   // the window rows, read (like q) only after the wait
           ensure_wait();
           if (my_row < a.w) my_off = win_off + (long long)my_row * a.win.sn;
@@ -443,7 +445,7 @@ __global__ void __launch_bounds__(SkCfg<D, MT>::NT, 1)
       seg_range(sgi, u, lt0, lt1);
       seg_tiles = lt1 - lt0;
       seg_lt0 = lt0;
-      if (a.has_win) {   // window position of rows 16 wm + gq and + 8
+      if (WIN) {   // window position of rows 16 wm + gq and + 8
         const int r0 = (u % a.row_blocks) * C::ROWS + wm * 16 + gq;
         tA = r0 % a.w;
         tB = (r0 + 8) % a.w;
@@ -517,7 +519,7 @@ __global__ void __launch_bounds__(SkCfg<D, MT>::NT, 1)
       // Rows left out of the tile get -inf.  Scores stay unscaled here: the
       // scale (> 0) is folded into the exponent below, so the maximum is
       // taken on raw scores and converted once per row.
-      if (a.has_win && seg_lt0 + i == a.tph) {   // the window: causal
+      if (WIN && seg_lt0 + i == a.tph) {   // the window: causal
 #pragma unroll
         for (int j = 0; j < C::NT8; ++j)
 #pragma unroll

@@ -388,6 +388,40 @@ def prepare_sparse_verify_attn(q, kv, h_kv, n, idx, scale, o, lse, ws,
     return call
 
 
+def prepare_sparse_verify_attn_window(q, kv, h_kv, n, idx, win, scale, o, lse,
+                                      ws, stream=None, flags=0):
+    _attn_checks(q, o, lse)
+    b, h_q, w, d = q.shape
+    fn = load().dustin_sparse_verify_attn_window
+    kvc, winc = DustinKV.from_buffer_copy(kv), DustinKV.from_buffer_copy(win)
+    args = (b, h_q, h_kv, d, w, n, idx.shape[1], q.data_ptr(),
+            ctypes.addressof(kvc), idx.data_ptr(), ctypes.addressof(winc),
+            float(scale), o.data_ptr(), lse.data_ptr(), _ptr(ws),
+            0 if ws is None else ws.numel(), int(flags), _stream(stream, q.device))
+
+    def call():
+        _check(fn(*args))
+    call.keep = (kvc, winc)
+    return call
+
+
+def prepare_full_verify_attn_window(q, kv, h_kv, n, win, scale, o, lse, ws,
+                                    stream=None, flags=0):
+    _attn_checks(q, o, lse)
+    b, h_q, w, d = q.shape
+    fn = load().dustin_full_verify_attn_window
+    kvc, winc = DustinKV.from_buffer_copy(kv), DustinKV.from_buffer_copy(win)
+    args = (b, h_q, h_kv, d, w, n, q.data_ptr(), ctypes.addressof(kvc),
+            ctypes.addressof(winc), float(scale), o.data_ptr(), lse.data_ptr(),
+            _ptr(ws), 0 if ws is None else ws.numel(), int(flags),
+            _stream(stream, q.device))
+
+    def call():
+        _check(fn(*args))
+    call.keep = (kvc, winc)
+    return call
+
+
 def prepare_full_verify_attn(q, kv, h_kv, n, scale, o, lse, ws, stream=None,
                              flags=0):
     _attn_checks(q, o, lse)

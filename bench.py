@@ -308,6 +308,10 @@ def run_extras(rep, wl, dev, stream, L, args, t_attn, t_dense):
         return e0.elapsed_time(e1) * 1e3 / (reps * len(calls))
 
     t_sw = time_pass(sw, 5)
+    # All layers' sparse attention in one persistent launch.
+    ml = N.prepare_sparse_verify_attn_layers(
+        inp.q, kv, wl.hkv, wl.n, rep.idx, wl.scale, rep.o, rep.lse)
+    t_ml = time_pass([ml], 5) / L
     t_fw = time_pass(fw, 1) if not args.no_dense else None
     # Naive estimator: all h_q heads of each layer as that layer's scored
     # pairs (latest-token query, one row), one scoring call per layer.
@@ -320,6 +324,11 @@ def run_extras(rep, wl, dev, stream, L, args, t_attn, t_dense):
                                    wl.scale, s_out, ws, wl.n) for l in range(L)]
     t_naive_layer = time_pass(naive, 1)
     return {
+        "multi_layer_sparse_us_per_layer": t_ml,
+        "multi_layer_sparse_gbs": rep.bytes_sparse_launch() / (t_ml * 1e-6) / 1e9,
+        "multi_layer_note": (f"all {L} layers in one launch: only for callers that "
+                             "hold every layer's queries at once; the headline "
+                             "calls one launch per layer"),
         "window_sparse_us_per_layer": t_sw,
         "window_sparse_overhead_us": t_sw - t_attn,
         "window_dense_us_per_layer": t_fw,

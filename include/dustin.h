@@ -240,6 +240,27 @@ int dustin_sparse_verify_attn_window(int b, int h_q, int h_kv, int d, int w,
                                      float* lse, void* ws, size_t ws_bytes,
                                      unsigned flags, void* stream);
 
+/* Sparse verification attention of n_layers layers in one persistent
+ * launch: for each layer l, the call dustin_sparse_verify_attn(b, h_q, h_kv,
+ * d, w, n, k, q[l], &kv[l], idx, scale, o[l], lse[l]) with one index set
+ * for all layers.  For callers that hold several layers' queries at once
+ * (the layers of one model run one after another, so within a single
+ * forward pass only one layer is ready at a time).  The (layer, sequence,
+ * kv head, row block) units are dealt round-robin to one CTA per SM, which
+ * streams them back to back without draining its pipeline.
+ *   q, o, lse  host arrays [n_layers] of device pointers (as in the sparse
+ *              call); kv host array [n_layers] of descriptors, all paged or
+ *              all contiguous
+ *   flags      0 or DUSTIN_ATTN_KV_READY (accepted, no effect)
+ * No workspace.  Limits as the sparse call, and k <= 2048
+ * (DUSTIN_ERR_UNSUPPORTED); any number of layers (launches of up to 128).
+ * Not an API of the paper. */
+int dustin_sparse_verify_attn_layers(int n_layers, int b, int h_q, int h_kv, int d,
+                                     int w, int n, int k, const void* const* q,
+                                     const dustin_kv* kv, const int32_t* idx,
+                                     float scale, void* const* o, float* const* lse,
+                                     unsigned flags, void* stream);
+
 /* DUSTIN_ATTN_KV_READY: the caller guarantees that idx, the page table and
  * the K/V cache were complete before the kernel enqueued just before this
  * call on `stream` started (that kernel does not write them; q may be its

@@ -10,6 +10,7 @@
 
 #include "attn.cuh"
 #include "attn_streamk.cuh"
+#include "attn_multilayer.cuh"
 #include "dustin.h"
 #include "internal.h"
 
@@ -387,6 +388,7 @@ int dustin_device_status(uint32_t* flags) {
   unsigned f = 0;
   if ((e = take_attn_sparse_flags(&f)) != cudaSuccess ||
       (e = take_attn_dense_flags(&f)) != cudaSuccess ||
+      (e = take_attn_ml_flags(&f)) != cudaSuccess ||
       (e = take_score_flags(&f)) != cudaSuccess)
     return cuda_fail(e, "dustin_device_status");
   if (flags) *flags = f;
@@ -540,6 +542,73 @@ int dustin_sparse_verify_attn_window(int b, int h_q, int h_kv, int d, int w,
   if (!win) return fail(DUSTIN_ERR_INVALID_ARG, "dustin_sparse_verify_attn_window: win is NULL");
   return run_attn(false, b, h_q, h_kv, d, w, n, k, q, kv, idx, win, scale, o, lse,
                   ws, ws_bytes, flags, stream);
+}
+
+int dustin_sparse_verify_attn_layers(int n_layers, int b, int h_q, int h_kv, int d,
+                                     int w, int n, int k, const void* const* q,
+                                     const dustin_kv* kv, const int32_t* idx,
+                                     float scale, void* const* o, float* const* lse,
+                                     unsigned flags, void* stream) {
+  const char* what = "dustin_sparse_verify_attn_layers";
+  if (n_layers < 0) return fail(DUSTIN_ERR_SHAPE, "%s: n_layers=%d", what, n_layers);
+  int rc = check_attn_shape(b, h_q, h_kv, d, w, n, what);
+  if (rc) return rc;
+  if (k < 0 || k > n)
+    return fail(DUSTIN_ERR_SHAPE, "%s: k=%d must be in [0, n=%d]", what, k, n);
+  if (k > 2048)
+    return fail(DUSTIN_ERR_UNSUPPORTED, "%s: k=%d (at most 2048 per call)", what, k);
+  if (n_layers == 0 || b == 0) return DUSTIN_OK;
+  if (!q || !kv || !o || !lse)
+    return fail(DUSTIN_ERR_INVALID_ARG, "%s: q, kv, o and lse arrays are required", what);
+  if (k > 0 && !idx) return fail(DUSTIN_ERR_INVALID_ARG, "%s: idx is NULL", what);
+  if (idx && (reinterpret_cast<uintptr_t>(idx) & 3u))
+    return fail(DUSTIN_ERR_ALIGNMENT, "%s: idx needs 4-byte alignment", what);
+  if (!std::isfinite(scale) || !(scale > 0.f))
+    return fail(DUSTIN_ERR_INVALID_ARG, "%s: scale must be finite and > 0", what);
+  if (flags & ~DUSTIN_ATTN_KV_READY)
+    return fail(DUSTIN_ERR_INVALID_ARG, "%s: unknown flags 0x%x", what, flags);
+  const bool paged = kv[0].page_table != nullptr;
+  for (int l = 0; l < n_layers; ++l) {
+    if (!q[l] || !o[l] || !lse[l])
+      return fail(DUSTIN_ERR_INVALID_ARG, "%s: layer %d: q, o and lse are required", what, l);
+    if (!aligned16(q[l]) || !aligned16(o[l]) || (reinterpret_cast<uintptr_t>(lse[l]) & 3u))
+      return fail(DUSTIN_ERR_ALIGNMENT, "%s: layer %d: q/o need 16-byte, lse 4-byte alignment",
+                  what, l);
+    if ((rc = check_kv(&kv[l], b, n, d, true, what))) return rc;
+    if ((kv[l].page_table != nullptr) != paged)
+      return fail(DUSTIN_ERR_INVALID_ARG, "%s: layers mix paged and contiguous caches", what);
+  }
+  const AttnPlan p = plan_units(h_q, h_kv, w, b, k);
+  const long long slots = (long long)attn_slots(true, d, p.mt);
+  for (int l0 = 0; l0 < n_layers; l0 += kMlMaxLayers) {
+    const int nl = std::min(kMlMaxLayers, n_layers - l0);
+    AttnMlArgs a;
+    a.idx = idx;
+    a.layers = nl;
+    a.b = b;
+    a.hq = h_q;
+    a.hkv = h_kv;
+    a.w = w;
+    a.n = n;
+    a.k = k;
+    a.group = h_q / h_kv;
+    a.rows = a.group * w;
+    a.row_blocks = p.row_blocks;
+    a.units = (int)p.units;
+    a.tpu = p.tpu;
+    a.scale_log2 = scale * kLog2e;
+    for (int l = 0; l < nl; ++l) {
+      a.layer[l].q = static_cast<const __nv_bfloat16*>(q[l0 + l]);
+      a.layer[l].o = static_cast<__nv_bfloat16*>(o[l0 + l]);
+      a.layer[l].lse = lse[l0 + l];
+      a.layer[l].kv = to_view(kv[l0 + l]);
+    }
+    const long long items = (long long)nl * p.units;
+    const int grid = (int)std::min(slots, items);
+    cudaError_t e = launch_attn_ml(a, d, p.mt, paged, grid, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, what);
+  }
+  return DUSTIN_OK;
 }
 
 size_t dustin_full_verify_attn_workspace_size(int b, int h_q, int h_kv, int d,

@@ -52,6 +52,10 @@ cudaError_t launch_attn_sparse(const AttnArgs& a, int d, int mt, bool paged,
                                cudaStream_t st);
 cudaError_t launch_attn_dense(const AttnSkArgs& a, int d, int mt, bool paged,
                               cudaStream_t st);
+struct AttnMlArgs;
+cudaError_t launch_attn_ml(const AttnMlArgs& a, int d, int mt, bool paged, int grid,
+                           cudaStream_t st);
+cudaError_t take_attn_ml_flags(unsigned* flags);
 int occupancy_attn_sparse(int d, int mt);
 int occupancy_attn_dense(int d, int mt);
 cudaError_t take_attn_sparse_flags(unsigned* flags);

@@ -30,6 +30,7 @@ EXPORTS = (
     "dustin_sparse_verify_attn_window",
     "dustin_full_verify_attn_workspace_size", "dustin_full_verify_attn",
     "dustin_full_verify_attn_window",
+    "dustin_sparse_verify_attn_layers",
 )
 
 
@@ -98,6 +99,8 @@ def load(build_if_missing: bool = False, path: Optional[str] = None
                                                  F, P, P, P, S, U, P]),
         "dustin_full_verify_attn_window": (I, [I, I, I, I, I, I, P, P, P, F, P, P,
                                                P, S, U, P]),
+        "dustin_sparse_verify_attn_layers": (I, [I, I, I, I, I, I, I, I, P, P, P, F,
+                                                 P, P, U, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -320,6 +323,55 @@ def dustin_full_verify_attn_window(q: torch.Tensor, kv: DustinKV, h_kv: int,
         b, h_q, h_kv, d, w, n, q.data_ptr(), ctypes.byref(kv), ctypes.byref(win),
         float(scale), o.data_ptr(), lse.data_ptr(), _ptr(ws),
         0 if ws is None else ws.numel(), int(flags), _stream(stream, q.device)))
+
+
+def _layers_args(qs, kvs, idx, os, lses):
+    n_layers = len(qs)
+    if not (len(kvs) == len(os) == len(lses) == n_layers) or n_layers == 0:
+        raise ValueError("one q, kv, o and lse per layer")
+    for q, o, lse in zip(qs, os, lses):
+        _attn_checks(q, o, lse)
+        if q.shape != qs[0].shape:
+            raise ValueError("every layer's q has the same shape")
+    if idx.dtype != torch.int32 or not idx.is_contiguous() or idx.dim() != 2 \
+            or idx.shape[0] != qs[0].shape[0]:
+        raise ValueError("idx must be contiguous int32 [b][k]")
+    qa = (ctypes.c_void_p * n_layers)(*[q.data_ptr() for q in qs])
+    oa = (ctypes.c_void_p * n_layers)(*[o.data_ptr() for o in os])
+    la = (ctypes.c_void_p * n_layers)(*[t.data_ptr() for t in lses])
+    ka = (DustinKV * n_layers)(*kvs)
+    return qa, ka, oa, la
+
+
+def dustin_sparse_verify_attn_layers(qs: Sequence[torch.Tensor],
+                                     kvs: Sequence[DustinKV], h_kv: int, n: int,
+                                     idx: torch.Tensor, scale: float,
+                                     os: Sequence[torch.Tensor],
+                                     lses: Sequence[torch.Tensor], stream=None,
+                                     flags: int = 0) -> None:
+    """The sparse call for several layers in one persistent launch (one
+    index set for all layers)."""
+    qa, ka, oa, la = _layers_args(qs, kvs, idx, os, lses)
+    b, h_q, w, d = qs[0].shape
+    _check(load().dustin_sparse_verify_attn_layers(
+        len(qs), b, h_q, h_kv, d, w, n, idx.shape[1], ctypes.addressof(qa),
+        ctypes.addressof(ka), idx.data_ptr(), float(scale), ctypes.addressof(oa),
+        ctypes.addressof(la), int(flags), _stream(stream, qs[0].device)))
+
+
+def prepare_sparse_verify_attn_layers(qs, kvs, h_kv, n, idx, scale, os, lses,
+                                      stream=None, flags=0):
+    qa, ka, oa, la = _layers_args(qs, kvs, idx, os, lses)
+    b, h_q, w, d = qs[0].shape
+    fn = load().dustin_sparse_verify_attn_layers
+    args = (len(qs), b, h_q, h_kv, d, w, n, idx.shape[1], ctypes.addressof(qa),
+            ctypes.addressof(ka), idx.data_ptr(), float(scale), ctypes.addressof(oa),
+            ctypes.addressof(la), int(flags), _stream(stream, qs[0].device))
+
+    def call():
+        _check(fn(*args))
+    call.keep = (qa, ka, oa, la)
+    return call
 
 
 # ------------------------------------------------------------------ misc

@@ -98,6 +98,23 @@ def test_attention_validation(lib):
     assert sparse(lib, b=0, q=None, o=None, lse=None)[0] == 0
 
 
+def test_multi_layer_validation(lib):
+    qa = (ctypes.c_void_p * 2)(FAKE, FAKE)
+    ka = (native.DustinKV * 2)(kv(), kv())
+    la = (ctypes.c_void_p * 2)(FAKE, FAKE)
+
+    def call(k=32, kvs=ka, n_layers=2):
+        return lib.dustin_sparse_verify_attn_layers(
+            n_layers, 1, 8, 2, 128, 4, 4096, k, ctypes.addressof(qa),
+            ctypes.addressof(kvs), FAKE, 0.1, ctypes.addressof(qa),
+            ctypes.addressof(la), 0, None)
+    assert call(k=3000) == 3                     # k above 2048
+    mixed = (native.DustinKV * 2)(kv(), kv(page_table=FAKE, page_size=16, ppseq=256,
+                                       pages=64))
+    assert call(kvs=mixed) == 1                  # paged and contiguous mixed
+    assert call(n_layers=0) == 0                 # nothing to do
+
+
 def test_score_and_select_validation(lib):
     heads = (ctypes.c_int32 * 1)(0)
     arr = (native.DustinKV * 1)(kv())

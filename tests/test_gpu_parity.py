@@ -209,6 +209,53 @@ def test_window_attention_paged_and_kv_ready():
     assert N.dustin_device_status() == 0
 
 
+# ---------------------------------------- several layers in one launch
+
+@pytest.mark.parametrize("shape,layers,paged", [
+    ((2, 28, 4, 128, 4, 700, 131), 3, False),
+    ((3, 40, 8, 128, 5, 1000, 333), 4, True),
+    ((1, 64, 4, 64, 5, 900, 450), 2, False),
+    ((4, 14, 2, 64, 4, 129, 0), 2, False),
+    ((48, 32, 8, 128, 2, 600, 300), 3, False),
+], ids=["3x-rows4", "4x-paged", "2x-d64", "k0", "many-units"])
+def test_multi_layer_launch_matches_per_layer_calls(shape, layers, paged):
+    """Every layer of the persistent multi-layer launch gives the same bits
+    as its own per-layer call (same tiles, same math and merge order), and
+    matches the oracle."""
+    b, hq, hkv, d, w, n, k = shape
+    idx = (I.random_sorted_indices(b, n, k, seed=41) if k else
+           torch.zeros((b, 0), dtype=torch.int32)).to(DEV)
+    qs, descs, keep, host = [], [], [], []
+    for l in range(layers):
+        q, kk, v = qkv(b, hq, hkv, d, w, n, seed=300 + l)
+        host.append((q, kk, v))
+        table = None
+        if paged:
+            kk, v, table = I.to_paged(kk, v, 16, seed=400 + l)
+            table = table.to(DEV)
+        q, kk, v = q.to(DEV), kk.to(DEV), v.to(DEV)
+        keep += [kk, v, table]
+        qs.append(q)
+        descs.append(N.kv_desc(kk, v, table))
+    os = [torch.full_like(q, float("nan")) for q in qs]
+    lses = [torch.full((b, hq, w), float("nan"), device=DEV) for _ in qs]
+    N.dustin_sparse_verify_attn_layers(qs, descs, hkv, n, idx, 0.1, os, lses)
+    H.sync()
+    assert N.dustin_device_status() == 0
+    ws = N.workspace(N.dustin_sparse_verify_attn_workspace_size(b, hq, hkv, d, w, k), DEV)
+    for l in range(layers):
+        o1 = torch.full_like(qs[l], float("nan"))
+        l1 = torch.full((b, hq, w), float("nan"), device=DEV)
+        N.dustin_sparse_verify_attn(qs[l], descs[l], hkv, n, idx, 0.1, o1, l1, ws)
+        H.sync()
+        if k == 0 or N.dustin_sparse_verify_attn_workspace_size(b, hq, hkv, d, w, k) <= 1:
+            assert torch.equal(os[l], o1) and torch.equal(lses[l], l1)
+        q, kk, v = host[l]
+        o_ref, l_ref = O.verify_attention(H.f64(q), H.f64(kk), H.f64(v),
+                                          idx.cpu().numpy(), 0.1)
+        H.assert_attn_close(os[l], lses[l], o_ref, l_ref)
+
+
 def test_sparse_with_all_positions_matches_full():
     b, hq, hkv, d, w, n = 2, 16, 2, 128, 4, 777
     q, kk, v = qkv(b, hq, hkv, d, w, n, seed=5)

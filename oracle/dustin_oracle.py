@@ -347,6 +347,59 @@ def full_verify_attention(q, keys, values, scale):
     return verify_attention(q, keys, values, None, scale)
 
 
+# ---------------------------------------------- Quest page scoring (baseline)
+
+def quest_page_stats(keys: np.ndarray, page: int) -> np.ndarray:
+    """Per-page key statistics of the Quest baseline ([Notes] section 1 and
+    related work: query-aware selection that scores KV pages from cheap
+    per-channel min/max key statistics instead of the exact q K^T).
+
+    keys [b][hkv][n][d]; pages of `page` consecutive positions (the last one
+    may be short).  Returns [b][hkv][P][2][d]: channel-wise minimum, then
+    maximum, over the page's positions."""
+    keys = np.asarray(keys, np.float64)
+    b, hkv, n, d = keys.shape
+    n_pages = (n + page - 1) // page
+    out = np.zeros((b, hkv, n_pages, 2, d))
+    for p in range(n_pages):
+        blk = keys[:, :, p * page:min(n, (p + 1) * page)]
+        out[:, :, p, 0] = blk.min(axis=2)
+        out[:, :, p, 1] = blk.max(axis=2)
+    return out
+
+
+def quest_page_scores(q: np.ndarray, stats: np.ndarray) -> np.ndarray:
+    """Quest's page score for each query head: the largest value q . k can
+    take for a key inside the page's channel-wise box,
+      score[b][h][p] = sum_c max(q_c * min_c, q_c * max_c),
+    with the stats of kv head h // (hq // hkv).  q [b][hq][d]; stats as
+    ``quest_page_stats``.  Returns [b][hq][P]."""
+    q = np.asarray(q, np.float64)
+    stats = np.asarray(stats, np.float64)
+    b, hq, d = q.shape
+    hkv = stats.shape[1]
+    group = hq // hkv
+    out = np.zeros((b, hq, stats.shape[2]))
+    for h in range(hq):
+        st = stats[:, h // group]                       # [b][P][2][d]
+        qh = q[:, h][:, None, :]                        # [b][1][d]
+        out[:, h] = np.maximum(qh * st[:, :, 0], qh * st[:, :, 1]).sum(axis=-1)
+    return out
+
+
+def quest_select_pages(scores: np.ndarray, n_pages_kept: int) -> np.ndarray:
+    """Top pages per (sequence, head), in ascending page order ([b][hq][m]),
+    with the tie order of ``rank_order``."""
+    scores = np.asarray(scores, np.float64)
+    b, hq, n_pages = scores.shape
+    m = min(n_pages_kept, n_pages)
+    out = np.zeros((b, hq, m), dtype=np.int64)
+    for bi in range(b):
+        for h in range(hq):
+            out[bi, h] = np.sort(topk(scores[bi, h], m))
+    return out
+
+
 def round_to_bf16(x: np.ndarray) -> np.ndarray:
     """Round float64 values to the nearest bf16 (ties to even), returned as
     float64.  Used only to present oracle outputs in the output precision."""

@@ -447,3 +447,60 @@ def test_bf16_rounding_helper():
     x = np.array([1.0, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -9, -2.5, 0.0, 1e-3])
     torch_round = torch.from_numpy(x).to(torch.bfloat16).double().numpy()
     np.testing.assert_array_equal(O.round_to_bf16(x), torch_round)
+
+
+# --------------------------------------------- Quest page scoring (baseline)
+
+def test_quest_stats_bound_every_key_of_the_page():
+    """Invariant: q . k <= score of k's page for every key (the box bound),
+    with equality when the page holds one key; stats do not depend on the
+    order of the keys inside a page."""
+    rng = np.random.default_rng(51)
+    b, hq, hkv, n, d, page = 2, 4, 2, 53, 8, 16
+    k = rng.standard_normal((b, hkv, n, d))
+    q = rng.standard_normal((b, hq, d))
+    st = O.quest_page_stats(k, page)
+    sc = O.quest_page_scores(q, st)
+    assert st.shape == (b, hkv, 4, 2, d) and sc.shape == (b, hq, 4)
+    for bi in range(b):
+        for h in range(hq):
+            dots = k[bi, h // 2] @ q[bi, h]
+            for j in range(n):
+                assert dots[j] <= sc[bi, h, j // page] + 1e-12
+            # the short last page (53 = 3 * 16 + 5) has its own box
+            last = k[bi, h // 2, 48:]
+            assert np.allclose(st[bi, h // 2, 3, 0], last.min(axis=0))
+    perm = np.concatenate([rng.permutation(16) + 16 * p for p in range(3)] +
+                          [48 + rng.permutation(5)])
+    np.testing.assert_array_equal(O.quest_page_stats(k[:, :, perm], page), st)
+    one = O.quest_page_stats(k, 1)
+    np.testing.assert_allclose(O.quest_page_scores(q, one)[:, 0],
+                               np.einsum("bnd,bd->bn", k[:, 0], q[:, 0]),
+                               atol=1e-12)
+
+
+def test_quest_scores_closed_forms():
+    rng = np.random.default_rng(52)
+    k = rng.standard_normal((1, 1, 32, 6))
+    st = O.quest_page_stats(k, 16)
+    for c in range(6):
+        e = np.zeros((1, 1, 6))
+        e[0, 0, c] = 1.0                     # unit query: the page maximum
+        np.testing.assert_allclose(O.quest_page_scores(e, st)[0, 0],
+                                   [k[0, 0, :16, c].max(), k[0, 0, 16:, c].max()])
+        np.testing.assert_allclose(O.quest_page_scores(-e, st)[0, 0],
+                                   [-k[0, 0, :16, c].min(), -k[0, 0, 16:, c].min()])
+    # brute force over the box corners: the score is the largest q . x over
+    # x in the box, attained at a corner
+    q = rng.standard_normal((1, 1, 6))
+    lo, hi = st[0, 0, 0, 0], st[0, 0, 0, 1]
+    best = max(q[0, 0] @ np.where(np.array(bits), hi, lo)
+               for bits in itertools.product([0, 1], repeat=6))
+    assert O.quest_page_scores(q, st)[0, 0, 0] == pytest.approx(best, abs=1e-12)
+
+
+def test_quest_page_selection():
+    sc = np.array([[[0.5, 2.0, 2.0, -1.0, 3.0]]])
+    np.testing.assert_array_equal(O.quest_select_pages(sc, 3), [[[1, 2, 4]]])
+    np.testing.assert_array_equal(O.quest_select_pages(sc, 2), [[[1, 4]]])
+    np.testing.assert_array_equal(O.quest_select_pages(sc, 9), [[[0, 1, 2, 3, 4]]])

@@ -94,6 +94,17 @@ def _window_attention_not_causal(q, keys, values, idx, k_win, v_win, scale):
     return out, lse
 
 
+def _quest_scores_max_only(q, stats):
+    # uses the channel maxima whatever the sign of q_c
+    q = np.asarray(q, np.float64)
+    stats = np.asarray(stats, np.float64)
+    group = q.shape[1] // stats.shape[1]
+    out = np.zeros((q.shape[0], q.shape[1], stats.shape[2]))
+    for h in range(q.shape[1]):
+        out[:, h] = (q[:, h][:, None, :] * stats[:, h // group, :, 1]).sum(axis=-1)
+    return out
+
+
 ORIG = {name: getattr(O, name) for name in (
     "score_heads", "hybrid_scores", "softmax")}
 
@@ -117,6 +128,9 @@ MUTATIONS = [
     ("verify_attention_window", _window_attention_not_causal,
      [pins.test_window_attention_matches_sdpa_with_a_causal_window_mask,
       pins.test_window_attention_without_history_is_causal_self_attention]),
+    ("quest_page_scores", _quest_scores_max_only,
+     [pins.test_quest_stats_bound_every_key_of_the_page,
+      pins.test_quest_scores_closed_forms]),
     ("softmax", _softmax_transposed,
      [lambda: pins.test_dense_attention_matches_torch_sdpa(2, 4, 2, 3, 37, 16)]),
 ]

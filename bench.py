@@ -323,6 +323,30 @@ def run_extras(rep, wl, dev, stream, L, args, t_attn, t_dense):
     naive = [N.prepare_score_heads(q_all, [N.kv_desc(inp.k[l])] * hq, heads,
                                    wl.scale, s_out, ws, wl.n) for l in range(L)]
     t_naive_layer = time_pass(naive, 1)
+    # Quest-16: page statistics (kept up to date at append time in Quest, so
+    # timed apart) and, per step and layer, page scores for every query head
+    # (latest-token query) plus the top k/16 pages per (sequence, head).
+    page = 16
+    n_pages = (wl.n + page - 1) // page
+    nbuf = min(8, L)
+    stats = [N.dustin_quest_page_stats(kv[l], wl.b, wl.hkv, wl.d, wl.n, page,
+                                       device=dev) for l in range(nbuf)]
+    t_stats = time_pass([lambda l=l: N.dustin_quest_page_stats(
+        kv[l], wl.b, wl.hkv, wl.d, wl.n, page, stats=stats[l]) for l in range(nbuf)], 2)
+    q_row = torch.randn((wl.b, hq, wl.d), generator=g, device=dev).to(torch.bfloat16)
+    scores = torch.empty((wl.b, hq, n_pages), device=dev)
+    keep = max(1, wl.k // page)
+    pidx = torch.empty((wl.b * hq, keep), dtype=torch.int32, device=dev)
+    sel = N.prepare_hybrid_topk(scores.view(wl.b * hq, n_pages), None, keep, 0, 0,
+                                1.0, -1, N.DUSTIN_NORM_NONE, pidx)
+    quest = []
+    for l in range(L):
+        quest.append(lambda l=l: N.dustin_quest_page_scores(q_row, stats[l % nbuf],
+                                                            wl.n, page, scores=scores))
+        quest.append(sel)
+    t_quest_layer = time_pass(quest, 1) * 2
+    t_qscore = time_pass(quest[0::2], 1)
+    t_qsel = time_pass([sel] * 8, 2)
     return {
         "multi_layer_sparse_us_per_layer": t_ml,
         "multi_layer_sparse_gbs": rep.bytes_sparse_launch() / (t_ml * 1e-6) / 1e9,
@@ -333,6 +357,16 @@ def run_extras(rep, wl, dev, stream, L, args, t_attn, t_dense):
         "window_sparse_overhead_us": t_sw - t_attn,
         "window_dense_us_per_layer": t_fw,
         "window_dense_overhead_us": (t_fw - t_dense) if (t_fw and t_dense) else None,
+        "quest16_estimator": {
+            "what": (f"page scores of all {hq} query heads (latest-token query) "
+                     f"over 16-position page min/max statistics, then the top "
+                     f"{keep} pages per (sequence, head), for each of {L} layers"),
+            "ms_per_step": t_quest_layer * L / 1e3,
+            "page_scores_ms_per_step": t_qscore * L / 1e3,
+            "page_select_ms_per_step": t_qsel * L / 1e3,
+            "ratio_to_dense": (t_quest_layer / t_dense) if t_dense else None,
+            "stats_build_us_per_layer": t_stats,
+        },
         "naive_estimator": {
             "what": (f"all {hq} target query heads of each of {L} layers scored "
                      "(latest-token query), one scoring call per layer; draft "

@@ -261,6 +261,32 @@ int dustin_sparse_verify_attn_layers(int n_layers, int b, int h_q, int h_kv, int
                                      float scale, void* const* o, float* const* lse,
                                      unsigned flags, void* stream);
 
+/* ------------------------------------------------------------------------
+ * Quest page scoring: the page-level baseline selector of the comparison
+ * ([Notes] section 1 and related work; "Quest-16" in Fig. 8).  Not part of
+ * Dustin; for measurements beside it.
+ *
+ * dustin_quest_page_stats: per page of `page` consecutive positions (the
+ * last may be short), the channel-wise minimum and maximum of the keys:
+ *   stats bf16 [b][h_kv][P][2][d], P = ceil(n / page), minimum row first;
+ *   dustin_quest_stats_size() bytes, 16-byte aligned.
+ * kv: keys only (v unused), contiguous or paged.  In Quest the statistics
+ * are kept up to date as tokens are appended, not rebuilt every step.
+ *
+ * dustin_quest_page_scores: for one query row per head, q bf16 [b][h_q][d],
+ *   scores[b][h][p] = sum_c max(q[b][h][c] * min_c, q[b][h][c] * max_c)
+ * with the stats of kv head h / (h_q / h_kv): the largest q . k over the
+ * page's channel box.  scores fp32 [b][h_q][P].  The top pages per (b, h)
+ * come from dustin_hybrid_topk on scores viewed as b*h_q rows of P (alpha
+ * 1, s_target NULL, norm NONE, no protected positions).
+ * At most 64 query heads per kv head. */
+size_t dustin_quest_stats_size(int b, int h_kv, int d, int n, int page);
+int dustin_quest_page_stats(int b, int h_kv, int d, int n, int page,
+                            const dustin_kv* kv, void* stats, void* stream);
+int dustin_quest_page_scores(int b, int h_q, int h_kv, int d, int n, int page,
+                             const void* q, const void* stats, float* scores,
+                             void* stream);
+
 /* DUSTIN_ATTN_KV_READY: the caller guarantees that idx, the page table and
  * the K/V cache were complete before the kernel enqueued just before this
  * call on `stream` started (that kernel does not write them; q may be its

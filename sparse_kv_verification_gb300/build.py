@@ -22,7 +22,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libdustin.so")
 
 SOURCES = ["api.cu", "score.cu", "select.cu", "attn_sparse.cu", "attn_dense.cu",
-           "attn_ml.cu"]
+           "attn_ml.cu", "quest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
          "-I" + INCLUDE, "-I" + CSRC]

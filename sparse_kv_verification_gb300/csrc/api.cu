@@ -389,6 +389,7 @@ int dustin_device_status(uint32_t* flags) {
   if ((e = take_attn_sparse_flags(&f)) != cudaSuccess ||
       (e = take_attn_dense_flags(&f)) != cudaSuccess ||
       (e = take_attn_ml_flags(&f)) != cudaSuccess ||
+      (e = take_quest_flags(&f)) != cudaSuccess ||
       (e = take_score_flags(&f)) != cudaSuccess)
     return cuda_fail(e, "dustin_device_status");
   if (flags) *flags = f;
@@ -608,6 +609,70 @@ int dustin_sparse_verify_attn_layers(int n_layers, int b, int h_q, int h_kv, int
     cudaError_t e = launch_attn_ml(a, d, p.mt, paged, grid, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, what);
   }
+  return DUSTIN_OK;
+}
+
+size_t dustin_quest_stats_size(int b, int h_kv, int d, int n, int page) {
+  if (b <= 0 || h_kv <= 0 || n < 0 || page <= 0 || (d != 64 && d != 128)) return 0;
+  const size_t pages = ((size_t)n + page - 1) / page;
+  return (size_t)b * h_kv * pages * 2 * d * sizeof(uint16_t);
+}
+
+int dustin_quest_page_stats(int b, int h_kv, int d, int n, int page,
+                            const dustin_kv* kv, void* stats, void* stream) {
+  const char* what = "dustin_quest_page_stats";
+  if (b < 0 || h_kv < 1 || n < 0 || page < 1)
+    return fail(DUSTIN_ERR_SHAPE, "%s: b=%d h_kv=%d n=%d page=%d", what, b, h_kv, n, page);
+  if (d != 64 && d != 128)
+    return fail(DUSTIN_ERR_UNSUPPORTED, "%s: d=%d (64 or 128)", what, d);
+  if (b == 0 || n == 0) return DUSTIN_OK;
+  if (!stats || !aligned16(stats))
+    return fail(DUSTIN_ERR_ALIGNMENT, "%s: stats must be 16-byte aligned", what);
+  int rc = check_kv(kv, b, n, d, false, what);
+  if (rc) return rc;
+  QuestArgs a{};
+  a.kv = to_view(*kv);
+  a.stats = static_cast<__nv_bfloat16*>(stats);
+  a.b = b;
+  a.hkv = h_kv;
+  a.n = n;
+  a.page = page;
+  a.n_pages = (n + page - 1) / page;
+  cudaError_t e = launch_quest_stats(a, d, kv->page_table != nullptr, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  return DUSTIN_OK;
+}
+
+int dustin_quest_page_scores(int b, int h_q, int h_kv, int d, int n, int page,
+                             const void* q, const void* stats, float* scores,
+                             void* stream) {
+  const char* what = "dustin_quest_page_scores";
+  if (b < 0 || h_q < 1 || h_kv < 1 || h_q % h_kv || n < 0 || page < 1)
+    return fail(DUSTIN_ERR_SHAPE, "%s: b=%d h_q=%d h_kv=%d n=%d page=%d", what, b, h_q,
+                h_kv, n, page);
+  if (d != 64 && d != 128)
+    return fail(DUSTIN_ERR_UNSUPPORTED, "%s: d=%d (64 or 128)", what, d);
+  if (h_q / h_kv > 64)
+    return fail(DUSTIN_ERR_UNSUPPORTED, "%s: more than 64 query heads per kv head", what);
+  if (b == 0 || n == 0) return DUSTIN_OK;
+  if (!q || !stats || !scores)
+    return fail(DUSTIN_ERR_INVALID_ARG, "%s: q, stats and scores are required", what);
+  if (!aligned16(stats) || (reinterpret_cast<uintptr_t>(q) & 1u) ||
+      (reinterpret_cast<uintptr_t>(scores) & 3u))
+    return fail(DUSTIN_ERR_ALIGNMENT, "%s: stats 16-byte, q 2-byte, scores 4-byte aligned",
+                what);
+  QuestArgs a{};
+  a.stats_in = static_cast<const __nv_bfloat16*>(stats);
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.scores = scores;
+  a.b = b;
+  a.hq = h_q;
+  a.hkv = h_kv;
+  a.n = n;
+  a.page = page;
+  a.n_pages = (n + page - 1) / page;
+  cudaError_t e = launch_quest_scores(a, d, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, what);
   return DUSTIN_OK;
 }
 

@@ -33,6 +33,19 @@ int score_chunk();
 cudaError_t launch_score(const ScoreArgs& a, int d, bool paged, cudaStream_t st);
 cudaError_t take_score_flags(unsigned* flags);
 
+// ---- Quest page scoring (baseline selector)
+struct QuestArgs {
+  KvView kv;                     // keys (stats pass)
+  __nv_bfloat16* stats;          // [b][hkv][P][2][d] out (stats pass)
+  const __nv_bfloat16* stats_in; // the same, in (score pass)
+  const __nv_bfloat16* q;        // [b][hq][d] (score pass)
+  float* scores;                 // [b][hq][P] (score pass)
+  int b, hq, hkv, n, page, n_pages;
+};
+cudaError_t launch_quest_stats(const QuestArgs& a, int d, bool paged, cudaStream_t st);
+cudaError_t launch_quest_scores(const QuestArgs& a, int d, cudaStream_t st);
+cudaError_t take_quest_flags(unsigned* flags);
+
 // ---- selection
 struct SelectArgs {
   const float* sd;

@@ -31,6 +31,8 @@ EXPORTS = (
     "dustin_full_verify_attn_workspace_size", "dustin_full_verify_attn",
     "dustin_full_verify_attn_window",
     "dustin_sparse_verify_attn_layers",
+    "dustin_quest_stats_size", "dustin_quest_page_stats",
+    "dustin_quest_page_scores",
 )
 
 
@@ -101,6 +103,9 @@ def load(build_if_missing: bool = False, path: Optional[str] = None
                                                P, S, U, P]),
         "dustin_sparse_verify_attn_layers": (I, [I, I, I, I, I, I, I, I, P, P, P, F,
                                                  P, P, U, P]),
+        "dustin_quest_stats_size": (S, [I, I, I, I, I]),
+        "dustin_quest_page_stats": (I, [I, I, I, I, I, P, P, P]),
+        "dustin_quest_page_scores": (I, [I, I, I, I, I, I, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -372,6 +377,40 @@ def prepare_sparse_verify_attn_layers(qs, kvs, h_kv, n, idx, scale, os, lses,
         _check(fn(*args))
     call.keep = (qa, ka, oa, la)
     return call
+
+
+# ------------------------------------------------ Quest page scoring baseline
+
+def dustin_quest_page_stats(kv: DustinKV, b: int, h_kv: int, d: int, n: int,
+                            page: int, stats: Optional[torch.Tensor] = None,
+                            device=None, stream=None) -> torch.Tensor:
+    """Per-page channel min/max of the keys: bf16 [b][h_kv][P][2][d]."""
+    n_pages = (n + page - 1) // page
+    if stats is None:
+        stats = torch.empty((b, h_kv, n_pages, 2, d), dtype=torch.bfloat16,
+                            device=device)
+    _need_cuda(stats)
+    _check(load().dustin_quest_page_stats(b, h_kv, d, n, page, ctypes.byref(kv),
+                                          stats.data_ptr(),
+                                          _stream(stream, stats.device)))
+    return stats
+
+
+def dustin_quest_page_scores(q: torch.Tensor, stats: torch.Tensor, n: int,
+                             page: int, scores: Optional[torch.Tensor] = None,
+                             stream=None) -> torch.Tensor:
+    """q bf16 [b][h_q][d] (one row per head) -> fp32 [b][h_q][P]."""
+    _need_cuda(q, stats)
+    b, h_q, d = q.shape
+    h_kv, n_pages = stats.shape[1], stats.shape[2]
+    if q.dtype != torch.bfloat16 or not q.is_contiguous() or not stats.is_contiguous():
+        raise ValueError("q bf16 contiguous [b][h_q][d]; stats contiguous")
+    if scores is None:
+        scores = torch.empty((b, h_q, n_pages), device=q.device)
+    _check(load().dustin_quest_page_scores(b, h_q, h_kv, d, n, page, q.data_ptr(),
+                                           stats.data_ptr(), scores.data_ptr(),
+                                           _stream(stream, q.device)))
+    return scores
 
 
 # ------------------------------------------------------------------ misc

@@ -256,6 +256,42 @@ def test_multi_layer_launch_matches_per_layer_calls(shape, layers, paged):
         H.assert_attn_close(os[l], lses[l], o_ref, l_ref)
 
 
+# ---------------------------------------- Quest page scoring (baseline)
+
+@pytest.mark.parametrize("b,hq,hkv,d,n,page", [(2, 8, 2, 128, 1000, 16),
+                                               (3, 14, 2, 64, 777, 32),
+                                               (1, 64, 8, 128, 4096, 16)])
+def test_quest_page_scoring_parity(b, hq, hkv, d, n, page):
+    """Stats are exact (min/max of bf16 values); scores within fp32
+    rounding; the top pages picked by the selection kernel from the GPU
+    scores equal the oracle's page selection on the same scores; paged keys
+    give the same stats bits."""
+    g = I.generator(n + page)
+    k = (2.0 * torch.randn((b, hkv, n, d), generator=g)).to(torch.bfloat16)
+    q = torch.randn((b, hq, d), generator=g).to(torch.bfloat16)
+    dk, dq = k.to(DEV), q.to(DEV)
+    st = N.dustin_quest_page_stats(N.kv_desc(dk), b, hkv, d, n, page, device=DEV)
+    sc = N.dustin_quest_page_scores(dq, st, n, page)
+    H.sync()
+    st_ref = O.quest_page_stats(H.f64(k), page)
+    np.testing.assert_array_equal(H.f64(st), st_ref)
+    sc_ref = O.quest_page_scores(H.f64(q), st_ref)
+    np.testing.assert_allclose(H.f64(sc), sc_ref, rtol=1e-5, atol=1e-4)
+    n_pages = st.shape[2]
+    keep = max(1, n_pages // 8)
+    rows = sc.reshape(b * hq, n_pages).contiguous()
+    got = H.select(rows, None, keep, 0, 0, 1.0, -1, 0)
+    want = O.quest_select_pages(H.f64(sc), keep).reshape(b * hq, -1)
+    np.testing.assert_array_equal(got.cpu().numpy(), want)
+    pk, _, table = I.to_paged(k, None, 16, seed=5)
+    dpk, dtable = pk.to(DEV), table.to(DEV)     # alive while the kernel runs
+    st_p = N.dustin_quest_page_stats(N.kv_desc(dpk, None, dtable), b,
+                                     hkv, d, n, page, device=DEV)
+    H.sync()
+    assert torch.equal(st, st_p)
+    assert N.dustin_device_status() == 0
+
+
 def test_sparse_with_all_positions_matches_full():
     b, hq, hkv, d, w, n = 2, 16, 2, 128, 4, 777
     q, kk, v = qkv(b, hq, hkv, d, w, n, seed=5)

@@ -143,6 +143,18 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src,
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
+// Tiled TMA load of a 3-D box (coordinates in elements, innermost first)
+// through the tensor map at `map` (a __grid_constant__ kernel parameter),
+// completing on `bar`.  The innermost coordinate times the element size
+// must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, int x, int y,
+                                            int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
 // Arrives on `bar` once every cp.async this thread issued so far has landed
 // (the barrier's expected count includes this arrival).
 __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {

@@ -13,6 +13,9 @@
 // Pass 2 (score_reduce_kernel): combines the chunk statistics into each
 // row's log2-sum-exp and writes S[b][j] = sum_{p,r} 2^(l - lse2), summed
 // in a fixed order (pair-major, then row) in fp32.
+#include <cuda.h>
+
+#include <algorithm>
 #include <atomic>
 #include <cstdio>
 #include <mutex>
@@ -238,8 +241,344 @@ __global__ void __launch_bounds__(256) score_reduce_kernel(const ScoreArgs a) {
   }
 }
 
+// ---- Contiguous key caches: the logits pass on TMA.
+//
+// A persistent kernel (one CTA per SM for d = 128, two for d = 64) takes the
+// work items (pair, sequence, chunk) round-robin.  One producer warp loads
+// each item's query rows (cp.async, handed over through q_full / q_empty)
+// and, from lane 0, each 64-position tile of keys with tiled TMA loads of
+// 64 x 64 boxes (one per 64 channels) into 128B-swizzled stages; the
+// tensor map of a pair views its kv head of the cache as [b][n][d], so rows
+// past n come back as zeros.  Four consumer warps take 16 positions each per
+// tile, as in the cp.async kernel, and release the stage through its
+// "empty" mbarrier.  Every wait is bounded and raises flag 0x4 on timeout.
+struct ScoreTmaArgs {
+  ScoreArgs s;
+  CUtensorMap maps[kMaxPairs];   // per pair: kv head kv_head as [b][n][d]
+};
+
+// Build-time tunables: TMA pipeline depth per CTA (several CTAs share an
+// SM, each consuming its own tile).
+#ifndef DUSTIN_SCORE_STAGES128
+#define DUSTIN_SCORE_STAGES128 3
+#endif
+#ifndef DUSTIN_SCORE_STAGES64
+#define DUSTIN_SCORE_STAGES64 4
+#endif
+
+template <int D>
+struct TmaCfg {
+  static constexpr int STAGES = D == 128 ? DUSTIN_SCORE_STAGES128 : DUSTIN_SCORE_STAGES64;
+  static constexpr int HALVES = D / 64;
+  static constexpr int TILE_BYTES = kTile * D * 2;
+  static constexpr int Q_BYTES = 16 * D * 2;
+  static constexpr int OFF_Q = STAGES * TILE_BYTES;          // 1 KB multiple
+  static constexpr int OFF_RED = OFF_Q + Q_BYTES;
+  static constexpr int OFF_BAR = OFF_RED + kWarps * 16 * 8;
+  static constexpr int NBARS = 2 * STAGES + 2;
+  static constexpr int SMEM = OFF_BAR + NBARS * 8 + 1024;    // + alignment slack
+  static constexpr int NT = (kWarps + 1) * 32;
+};
+
+template <int D>
+__global__ void __launch_bounds__(TmaCfg<D>::NT)
+    score_logits_tma_kernel(const __grid_constant__ ScoreTmaArgs ta) {
+  using C = ScoreCfg<D>;
+  using T = TmaCfg<D>;
+  const ScoreArgs& a = ta.s;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // The 128B swizzle pattern is a function of the address: stages start on
+  // 1 KB boundaries.
+  unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  unsigned char* sQ = smem + T::OFF_Q;
+  float2* red = reinterpret_cast<float2*>(smem + T::OFF_RED);
+  const uint32_t bar0 = smem_u32(smem + T::OFF_BAR);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (T::STAGES + s); };
+  const uint32_t q_full = bar0 + 8u * (2 * T::STAGES);
+  const uint32_t q_empty = q_full + 8u;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tpi = a.chunk / kTile;
+  const long long n_items = (long long)a.n_pairs * a.b * a.nchunks;
+  struct Item {
+    int p, bb, c;
+  };
+  auto item_of = [&](long long it) {
+    Item x;
+    x.c = (int)(it % a.nchunks);
+    x.bb = (int)((it / a.nchunks) % a.b);
+    x.p = (int)(it / ((long long)a.nchunks * a.b));
+    return x;
+  };
+
+  griddep_wait();
+  griddep_launch_dependents();
+  if (tid == 0) {
+    for (int s = 0; s < T::STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), kWarps);
+    }
+    mbar_init(q_full, 32);
+    mbar_init(q_empty, kWarps);
+    mbar_fence_init();
+  }
+  __syncthreads();
+
+  if (warp == kWarps) {
+    // ============================ producer warp ============================
+    int t = 0, k = 0;
+    bool ok_run = true;
+    for (long long it = blockIdx.x; it < n_items && ok_run; it += gridDim.x, ++k) {
+      const Item x = item_of(it);
+      if (k > 0 && !mbar_wait(q_empty, (k - 1) & 1, kWaitLimitCycles)) {
+        if (lane == 0) atomicOr(&g_score_dev_flags, 4u);
+        break;
+      }
+      const __nv_bfloat16* qb = a.q + ((long long)x.p * a.b + x.bb) * a.rows * D;
+      for (int i = lane; i < 16 * C::CPR; i += 32) {
+        const int r = i / C::CPR, ch = i % C::CPR;
+        const bool ok = r < a.rows;
+        cp_async_16(smem_u32(sQ + swz<D>(r, ch)), qb + (ok ? r * D + ch * 8 : 0),
+                    ok ? 16 : 0);
+      }
+      cp_async_mbar_arrive(q_full);
+      const void* map = &ta.maps[x.p];
+      for (int tt = 0; tt < tpi; ++tt, ++t) {
+        const int st = t % T::STAGES;
+        if (t >= T::STAGES &&
+            !mbar_wait(empty_bar(st), ((t / T::STAGES) & 1) ^ 1, kWaitLimitCycles)) {
+          if (lane == 0) atomicOr(&g_score_dev_flags, 4u);
+          ok_run = false;
+          break;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(full_bar(st), T::TILE_BYTES);
+          const uint32_t dst = smem_u32(smem + st * T::TILE_BYTES);
+          const int j0 = x.c * a.chunk + tt * kTile;
+#pragma unroll
+          for (int h = 0; h < T::HALVES; ++h)
+            tma_load_3d(dst + h * (kTile * 128), map, h * 64, j0, x.bb, full_bar(st));
+        }
+        __syncwarp();
+      }
+    }
+    cp_async_wait<0>();
+    return;
+  }
+
+  // ============================ consumer warps =============================
+  const int gq = lane >> 2, tq = lane & 3;
+  int t = 0, k = 0;
+  bool dead = false;
+  auto wait_or_die = [&](uint32_t bar, uint32_t parity) {
+    if (dead) return;
+    if (!mbar_wait(bar, parity, kWaitLimitCycles)) {
+      dead = true;
+      if (lane == 0) atomicOr(&g_score_dev_flags, 4u);
+    }
+  };
+  for (long long it = blockIdx.x; it < n_items; it += gridDim.x, ++k) {
+    const Item x = item_of(it);
+    wait_or_die(q_full, k & 1);
+    uint32_t qf[C::KS][4];
+#pragma unroll
+    for (int ks = 0; ks < C::KS; ++ks)
+      ldmatrix_x4(smem_u32(sQ + swz<D>(lane & 15, ks * 2 + (lane >> 4))), qf[ks][0],
+                  qf[ks][1], qf[ks][2], qf[ks][3]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(q_empty);
+    const bool rowA = gq < a.rows, rowB = gq + 8 < a.rows;
+    float* outA = a.logits + (((long long)x.p * a.rows + gq) * a.b + x.bb) * a.n;
+    float* outB = a.logits + (((long long)x.p * a.rows + gq + 8) * a.b + x.bb) * a.n;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+    for (int tt = 0; tt < tpi; ++tt, ++t) {
+      const int st = t % T::STAGES;
+      wait_or_die(full_bar(st), (t / T::STAGES) & 1);
+      const unsigned char* tk = smem + st * T::TILE_BYTES;
+      const int p0 = x.c * a.chunk + tt * kTile;
+      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      const int r = warp * 16 + ((lane >> 4) << 3) + (lane & 7);
+#pragma unroll
+      for (int ks = 0; ks < C::KS; ++ks) {
+        // 16-byte chunk cg of row r, in the 64-channel box cg / 8, at its
+        // 128B-swizzled place.
+        const int cg = ks * 2 + ((lane >> 3) & 1);
+        const uint32_t addr = smem_u32(tk + (cg >> 3) * (kTile * 128) + r * 128 +
+                                       (((cg & 7) ^ (r & 7)) << 4));
+        uint32_t b0, b1, b2, b3;
+        ldmatrix_x4(addr, b0, b1, b2, b3);
+        mma_bf16(sc[0], qf[ks], b0, b1);
+        mma_bf16(sc[1], qf[ks], b2, b3);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_bar(st));
+      float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int j = p0 + warp * 16 + jj * 8 + 2 * tq + e;
+          const bool ok = j < a.n;
+          const float va = ok ? sc[jj][e] * a.scale_log2 : -INFINITY;
+          const float vb = ok ? sc[jj][e + 2] * a.scale_log2 : -INFINITY;
+          sc[jj][e] = va;
+          sc[jj][e + 2] = vb;
+          if (ok) {
+            if (rowA) outA[j] = va;
+            if (rowB) outB[j] = vb;
+          }
+          mx0 = fmaxf(mx0, va);
+          mx1 = fmaxf(mx1, vb);
+        }
+      }
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+      const float u0 = n0 == -INFINITY ? 0.f : n0, u1 = n1 == -INFINITY ? 0.f : n1;
+      float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        ps0 += ex2(sc[jj][0] - u0) + ex2(sc[jj][1] - u0);
+        ps1 += ex2(sc[jj][2] - u1) + ex2(sc[jj][3] - u1);
+      }
+      l0 = l0 * ex2(m0 - u0) + ps0;
+      l1 = l1 * ex2(m1 - u1) + ps1;
+      m0 = n0;
+      m1 = n1;
+    }
+    // Item end: per-row (max, sum) over the four warps.
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    if (tq == 0) {
+      red[warp * 16 + gq] = make_float2(m0, l0);
+      red[warp * 16 + gq + 8] = make_float2(m1, l1);
+    }
+    named_bar_sync(1, kWarps * 32);
+    if (tid < a.rows) {
+      float M = -INFINITY;
+      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red[w * 16 + tid].x);
+      const float u = M == -INFINITY ? 0.f : M;
+      float L = 0.f;
+      for (int w = 0; w < kWarps; ++w) {
+        const float2 v = red[w * 16 + tid];
+        L += v.y * ex2(v.x - u);
+      }
+      a.stats[(((long long)x.p * a.rows + tid) * a.b + x.bb) * a.nchunks + x.c] =
+          make_float2(M, L);
+    }
+    named_bar_sync(1, kWarps * 32);
+  }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against the driver library); null if unavailable.
+EncodeTiledFn encode_tiled() {
+  static std::atomic<EncodeTiledFn> fn{nullptr};
+  static std::atomic<int> tried{0};
+  EncodeTiledFn f = fn.load(std::memory_order_acquire);
+  if (f || tried.load()) return f;
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                       cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess && p) {
+    f = reinterpret_cast<EncodeTiledFn>(p);
+    fn.store(f, std::memory_order_release);
+  }
+  tried.store(1);
+  return f;
+}
+
+// Tensor maps of every pair; false if one cannot be encoded.
+template <int D>
+bool make_maps(const ScoreArgs& a, ScoreTmaArgs& ta) {
+  EncodeTiledFn enc = encode_tiled();
+  if (!enc) return false;
+  for (int p = 0; p < a.n_pairs; ++p) {
+    const KvView& kv = a.pairs[p].kv;
+    void* base = const_cast<__nv_bfloat16*>(kv.k + (long long)a.pairs[p].kv_head * kv.sh);
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)a.n, (cuuint64_t)a.b};
+    const cuuint64_t strides[2] = {(cuuint64_t)kv.sn * 2, (cuuint64_t)kv.sb * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)kTile, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (enc(&ta.maps[p], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  return true;
+}
+
+template <int D>
+cudaError_t run_score_tma(const ScoreArgs& a, cudaStream_t st, bool* used) {
+  using T = TmaCfg<D>;
+  *used = false;
+  static ScoreTmaArgs ta;   // large: kept off the stack; guarded below
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  ta.s = a;
+  if (!make_maps<D>(a, ta)) return cudaSuccess;
+  auto kern = score_logits_tma_kernel<D>;
+  static std::atomic<int> slots_memo[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) dev = 0;
+  int slots = slots_memo[dev].load(std::memory_order_relaxed);
+  if (slots <= 0) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM);
+    if (e != cudaSuccess) return e;
+    int occ = 0, sms = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, T::NT, T::SMEM);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    slots = std::max(1, occ) * std::max(1, sms);
+    slots_memo[dev].store(slots, std::memory_order_relaxed);
+  }
+  const long long items = (long long)a.n_pairs * a.b * a.nchunks;
+  const long long grid = std::min<long long>(items, slots);
+  e = launch_pdl(kern, dim3((unsigned)grid), dim3(T::NT), T::SMEM, st, ta);
+  if (e != cudaSuccess) return e;
+  note_launches(1);
+  *used = true;
+  return cudaSuccess;
+}
+
+template <int D, bool PAGED>
+cudaError_t run_score_cp(const ScoreArgs& a, cudaStream_t st);
+
 template <int D, bool PAGED>
 cudaError_t run_score(const ScoreArgs& a, cudaStream_t st) {
+  if constexpr (!PAGED) {
+    bool used = false;
+    cudaError_t e = run_score_tma<D>(a, st, &used);
+    if (e != cudaSuccess) return e;
+    if (used) {
+      dim3 g2((unsigned)((a.n + 1023) / 1024), (unsigned)a.b);
+      e = launch_pdl(score_reduce_kernel, g2, dim3(256), 0, st, a);
+      if (e == cudaSuccess) note_launches(1);
+      return e;
+    }
+  }
+  return run_score_cp<D, PAGED>(a, st);
+}
+
+template <int D, bool PAGED>
+cudaError_t run_score_cp(const ScoreArgs& a, cudaStream_t st) {
   using C = ScoreCfg<D>;
   auto kern = score_logits_kernel<D, PAGED>;
   cudaError_t e = cudaFuncSetAttribute(
@@ -257,7 +596,7 @@ cudaError_t run_score(const ScoreArgs& a, cudaStream_t st) {
 
 }  // namespace
 
-int score_chunk() { return 2048; }
+int score_chunk() { return 512; }
 
 cudaError_t launch_score(const ScoreArgs& a, int d, bool paged,
                          cudaStream_t st) {

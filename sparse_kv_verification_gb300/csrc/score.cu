@@ -216,17 +216,24 @@ __global__ void __launch_bounds__(256) score_reduce_kernel(const ScoreArgs a) {
   __shared__ float lse2[1024];
   const int bb = blockIdx.y;
   const int prs = a.n_pairs * a.rows;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   griddep_wait();
   griddep_launch_dependents();
-  for (int i = threadIdx.x; i < prs; i += blockDim.x) {
+  // Row i's log2-sum-exp from its chunk statistics: one warp per row, the
+  // lanes over the chunks.
+  for (int i = warp; i < prs; i += 8) {
     const float2* st = a.stats + ((long long)i * a.b + bb) * a.nchunks;
     float M = -INFINITY;
-    for (int c = 0; c < a.nchunks; ++c) M = fmaxf(M, st[c].x);
+    for (int c = lane; c < a.nchunks; c += 32) M = fmaxf(M, st[c].x);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     const float u = M == -INFINITY ? 0.f : M;
     float Z = 0.f;
-    for (int c = 0; c < a.nchunks; ++c) Z += st[c].y * ex2(st[c].x - u);
+    for (int c = lane; c < a.nchunks; c += 32) Z += st[c].y * ex2(st[c].x - u);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(0xffffffffu, Z, o);
     // An all-masked row contributes nothing.
-    lse2[i] = Z > 0.f ? u + log2f(Z) : INFINITY;
+    if (lane == 0) lse2[i] = Z > 0.f ? u + log2f(Z) : INFINITY;
   }
   __syncthreads();
   const long long base = (long long)blockIdx.x * 1024;

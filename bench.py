@@ -587,7 +587,7 @@ def run_ours(args):
                  "speedup_step": t_dense * L / 1e3 / t_ms}
 
     # ---- end to end: queries from pinned host memory in, outputs out.
-    # Copies run on two copy streams beside the compute stream, in chunks
+    # Copies run on two copy streams beside the compute stream, in 16 chunks
     # of layers: the scoring queries and the first layers' queries go in
     # first, each chunk's attention waits only for its own queries, and
     # each chunk's outputs go out as soon as they are written.  A step waits
@@ -597,7 +597,7 @@ def run_ours(args):
     if not args.no_e2e:
         inp = rep.inp
         L = rep.L
-        n_chunks = min(8, L)
+        n_chunks = min(16, L)
         bounds = [L * c // n_chunks for c in range(n_chunks + 1)]
         h_qt, h_qd = inp.q_t.cpu().pin_memory(), inp.q_d.cpu().pin_memory()
         h_q = rep.q_all.cpu().pin_memory()

@@ -292,6 +292,36 @@ def test_quest_page_scoring_parity(b, hq, hkv, d, n, page):
     assert N.dustin_device_status() == 0
 
 
+def test_multi_layer_launch_beyond_one_launch_of_layers():
+    """More layers than one launch carries (128): the call splits them into
+    launches; every layer still matches its own per-layer call bit for bit."""
+    b, hq, hkv, d, w, n, k, layers = 1, 4, 2, 64, 2, 100, 30, 130
+    idx = I.random_sorted_indices(b, n, k, seed=43).to(DEV)
+    g = I.generator(44)
+    qs = [torch.randn((b, hq, w, d), generator=g).to(torch.bfloat16).to(DEV)
+          for _ in range(layers)]
+    ks = [torch.randn((b, hkv, n, d), generator=g).to(torch.bfloat16).to(DEV)
+          for _ in range(layers)]
+    vs = [torch.randn((b, hkv, n, d), generator=g).to(torch.bfloat16).to(DEV)
+          for _ in range(layers)]
+    descs = [N.kv_desc(kk, vv) for kk, vv in zip(ks, vs)]
+    os = [torch.full_like(q, float("nan")) for q in qs]
+    lses = [torch.full((b, hq, w), float("nan"), device=DEV) for _ in qs]
+    N.dustin_sparse_verify_attn_layers(qs, descs, hkv, n, idx, 0.2, os, lses)
+    H.sync()
+    ws = N.workspace(N.dustin_sparse_verify_attn_workspace_size(b, hq, hkv, d, w, k), DEV)
+    for l in (0, 1, 127, 128, 129):
+        o1 = torch.full_like(qs[l], float("nan"))
+        l1 = torch.full((b, hq, w), float("nan"), device=DEV)
+        N.dustin_sparse_verify_attn(qs[l], descs[l], hkv, n, idx, 0.2, o1, l1, ws)
+        H.sync()
+        if N.dustin_sparse_verify_attn_workspace_size(b, hq, hkv, d, w, k) <= 1:
+            assert torch.equal(os[l], o1) and torch.equal(lses[l], l1)
+        else:
+            assert (os[l].float() - o1.float()).abs().max().item() <= 1e-2
+    assert N.dustin_device_status() == 0
+
+
 def test_sparse_with_all_positions_matches_full():
     b, hq, hkv, d, w, n = 2, 16, 2, 128, 4, 777
     q, kk, v = qkv(b, hq, hkv, d, w, n, seed=5)

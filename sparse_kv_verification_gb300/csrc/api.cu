@@ -119,6 +119,7 @@ struct AttnPlan {
   long long units;
   // sparse: positions split `splits` ways, `chunk` positions each.
   int splits, chunk;
+  bool wide;   // 32-bit row table (sparse)
   // dense: stream-K over `grid` CTAs; `split` when some unit is shared.
   long long grid;
   bool split;
@@ -136,19 +137,34 @@ AttnPlan plan_units(int hq, int hkv, int w, int b, int npos) {
   return p;
 }
 
-// Sparse: one CTA per unit; when the units leave SMs idle, the positions
-// of each unit are split into equal ranges (at most 2048 rows each, the
-// kernel's offset table) and merged by a combine kernel.
-AttnPlan plan_sparse(int b, int hq, int hkv, int d, int w, int k) {
+// Sparse: one CTA per unit; when the units leave SMs idle, or a unit has
+// more positions than one CTA's row table holds (8192, or 4096 with four
+// row tiles), the positions of each unit are split into equal ranges and
+// merged by a combine kernel.
+AttnPlan plan_sparse(int b, int hq, int hkv, int d, int w, int k, bool win) {
   AttnPlan p = plan_units(hq, hkv, w, b, k);
   const int tiles = (k + 63) / 64;
   p.splits = 1;
   p.chunk = 64;
+  p.wide = false;
   if (tiles > 0 && p.units > 0) {
     const long long slots = (long long)attn_slots(false, d, p.mt);
     long long s = p.units >= slots ? 1 : slots / p.units;
     s = std::min<long long>(s, tiles);
-    long long ct = std::min<long long>((tiles + s - 1) / s, 2048 / 64);
+    // Row table of one CTA (the kernel's TAB_BYTES): 64-bit offsets for up
+    // to cap64 tiles, 32-bit row codes (the WIDE variant; not with the
+    // window) for up to cap32.
+    const long long tab_bytes = p.mt == 4 ? 16384 : 32768;
+    const long long cap64 = tab_bytes / 8 / 64, cap32 = tab_bytes / 4 / 64;
+    long long ct = (tiles + s - 1) / s;
+    if (ct > cap64) {
+      if (win) {
+        ct = cap64;
+      } else {
+        p.wide = true;
+        ct = std::min(ct, cap32);
+      }
+    }
     p.splits = (int)((tiles + ct - 1) / ct);
     p.chunk = (int)(ct * 64);
   }
@@ -270,7 +286,9 @@ int run_attn(bool dense, int b, int hq, int hkv, int d, int w, int n, int k,
   const bool paged = kv->page_table != nullptr;
   cudaError_t e;
   if (!dense) {
-    const AttnPlan p = plan_sparse(b, hq, hkv, d, w, k);
+    if (paged && (long long)kv->num_pages * kv->page_size > 0x7fffffffLL)
+      return fail(DUSTIN_ERR_UNSUPPORTED, "%s: page pool of 2^31 rows or more", what);
+    const AttnPlan p = plan_sparse(b, hq, hkv, d, w, k, win != nullptr);
     if (p.units * p.splits > 0x7fffffffLL)
       return fail(DUSTIN_ERR_SHAPE, "%s: grid too large", what);
     const size_t need = p.workspace();
@@ -298,6 +316,7 @@ int run_attn(bool dense, int b, int hq, int hkv, int d, int w, int n, int k,
     a.scale_log2 = scale * kLog2e;
     a.kv_ready = (flags & DUSTIN_ATTN_KV_READY) ? 1 : 0;
     a.has_win = win ? 1 : 0;
+    a.wide = p.wide ? 1 : 0;
     if (win) a.win = to_view(*win);
     a.ws_o = need ? static_cast<float*>(ws) : nullptr;
     a.ws_ml = need ? reinterpret_cast<float2*>(static_cast<char*>(ws) + p.ws_o)
@@ -522,7 +541,9 @@ size_t dustin_sparse_verify_attn_workspace_size(int b, int h_q, int h_kv, int d,
   if (b <= 0 || h_q <= 0 || h_kv <= 0 || h_q % h_kv || w <= 0 || k < 0 ||
       (d != 64 && d != 128))
     return 0;
-  return plan_sparse(b, h_q, h_kv, d, w, k).workspace();
+  // Covers the call with and without the window merged in.
+  return std::max(plan_sparse(b, h_q, h_kv, d, w, k, false).workspace(),
+                  plan_sparse(b, h_q, h_kv, d, w, k, true).workspace());
 }
 
 int dustin_sparse_verify_attn(int b, int h_q, int h_kv, int d, int w, int n,

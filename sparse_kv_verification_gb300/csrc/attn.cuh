@@ -66,6 +66,7 @@ struct AttnArgs {
   KvView win;       // the window's own K/V [b][hkv][w][d] (has_win)
   int has_win;      // merge the window's causal block (last split only;
                     // selects the WIN instance of the kernel)
+  int wide;         // 32-bit row codes (selects the WIDE instance)
   float* ws_o;      // [blocks][splits][16 MT][D] (splits > 1)
   float2* ws_ml;    // [blocks][splits][16 MT]    (m in log2 units, l)
 };
@@ -120,9 +121,15 @@ struct AttnCfg {
   static constexpr int OFF_V = OFF_K + STAGES * TILE_BYTES;
   static constexpr int OFF_MASK = OFF_V + STAGES * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_MASK + STAGES * 8;   // 64-bit mask / stage
-  static constexpr int MAX_TAB = 2048;          // offset-table entries
+  // Row table of one CTA's positions: TAB_BYTES of shared memory holding
+  // either the 64-bit element offset of each row (TAB64 positions) or, in
+  // the WIDE kernel variant for longer ranges, a 32-bit row code (TAB32
+  // positions).  Four row tiles leave room for half as much.
+  static constexpr int TAB_BYTES = MT == 4 ? 16384 : 32768;
+  static constexpr int TAB64 = TAB_BYTES / 8;
+  static constexpr int TAB32 = TAB_BYTES / 4;
   static constexpr int OFF_TAB = OFF_BAR + 2 * STAGES * 8;
-  static constexpr int SMEM = OFF_TAB + MAX_TAB * 8;
+  static constexpr int SMEM = OFF_TAB + TAB_BYTES;
   static constexpr int MERGE_FLOATS = (WN - 1) * MT * 32 * (DT * 4 + 4);
   static_assert(MERGE_FLOATS * 4 <= 2 * STAGES * TILE_BYTES, "merge buffer");
   static_assert(SMEM <= 227 * 1024, "shared memory");
@@ -132,7 +139,7 @@ struct AttnCfg {
 static __device__ unsigned int g_attn_dev_flags;
 
 
-template <int D, int MT, bool PAGED, bool WIN>
+template <int D, int MT, bool PAGED, bool WIN, bool WIDE>
 __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
     verify_attn_kernel(const AttnArgs a) {
   using C = AttnCfg<D, MT>;
@@ -142,7 +149,8 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
   unsigned char* sV = smem + C::OFF_V;
   unsigned long long* sMask64 =
       reinterpret_cast<unsigned long long*>(smem + C::OFF_MASK);
-  long long* tab = reinterpret_cast<long long*>(smem + C::OFF_TAB);
+  long long* tab = reinterpret_cast<long long*>(smem + C::OFF_TAB);   // !WIDE
+  int* tab32 = reinterpret_cast<int*>(smem + C::OFF_TAB);              // WIDE
   const uint32_t bar0 = smem_u32(smem + C::OFF_BAR);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
@@ -211,27 +219,36 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
     }
     mbar_fence_init();
   }
-  // Offset table: element offset of each position's K/V row; -1 marks a
-  // row that failed a check.
+  // Row table: for each selected position, its element offset, or (WIDE)
+  // its row code: the position j in a contiguous cache, the pool row
+  // page * page_size + j % page_size in a paged one; -1 for a row that
+  // failed a check.
   {
     const int* idx_row = a.idx + (long long)bb * a.npos + p_begin;
     for (int i = tid; i < len; i += C::NT) {
       const int j = __ldg(idx_row + i);
       long long off = -1;
+      int code = -1;
       if (j < 0 || j >= a.n) {
         atomicOr(&g_attn_dev_flags, 1u);
       } else if constexpr (PAGED) {
         const int pg = __ldg(a.kv.page_table +
                              (long long)bb * a.kv.pages_per_seq + j / a.kv.page_size);
-        if (pg < 0 || pg >= a.kv.num_pages)
+        if (pg < 0 || pg >= a.kv.num_pages) {
           atomicOr(&g_attn_dev_flags, 2u);
-        else
+        } else {
           off = (long long)pg * a.kv.sb + (long long)g * a.kv.sh +
                 (long long)(j % a.kv.page_size) * a.kv.sn;
+          code = pg * a.kv.page_size + j % a.kv.page_size;   // < 2^31 (host check)
+        }
       } else {
         off = unit_off + (long long)j * a.kv.sn;
+        code = j;
       }
-      tab[i] = off;
+      if constexpr (WIDE)
+        tab32[i] = code;
+      else
+        tab[i] = off;
     }
   }
   cp_async_wait<0>();
@@ -259,7 +276,19 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
     // Element offset of tile row r (-1: leave the row out).
     auto row_offset = [&](int t, int r) -> long long {
       const int i = t * C::TILE + r;
-      return i < len ? tab[i] : -1;
+      if constexpr (!WIDE) {
+        return i < len ? tab[i] : -1;
+      } else {
+        const int code = i < len ? tab32[i] : -1;
+        if (code < 0) return -1;
+        if constexpr (PAGED) {
+          const int pg = code / a.kv.page_size;
+          return (long long)pg * a.kv.sb + (long long)g * a.kv.sh +
+                 (long long)(code - pg * a.kv.page_size) * a.kv.sn;
+        } else {
+          return unit_off + (long long)code * a.kv.sn;
+        }
+      }
     };
 
     // kv_ready: the first n_pre history tiles go out before this thread's

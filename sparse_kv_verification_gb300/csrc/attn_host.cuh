@@ -10,7 +10,7 @@
 namespace dustin {
 
 struct AttnHost {
-  template <int D, int MT, bool PAGED, bool WIN>
+  template <int D, int MT, bool PAGED, bool WIN, bool WIDE>
   static cudaError_t prepare() {
     using C = AttnCfg<D, MT>;
     static std::atomic<uint64_t> done{0};
@@ -21,7 +21,7 @@ struct AttnHost {
       static std::atomic<int> checked{0};
       if (checked.load() == 0) {
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, verify_attn_kernel<D, MT, PAGED, WIN>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, verify_attn_kernel<D, MT, PAGED, WIN, WIDE>);
         if (e != cudaSuccess) return e;
         const long long have = (long long)fa.numRegs * C::NT;
         const long long need = (long long)C::PRODUCER_REGS * C::NPW * 32 +
@@ -30,16 +30,16 @@ struct AttnHost {
       }
       if (checked.load() < 0) return cudaErrorInvalidConfiguration;
     }
-    return ensure_smem_attr(verify_attn_kernel<D, MT, PAGED, WIN>, C::SMEM, done);
+    return ensure_smem_attr(verify_attn_kernel<D, MT, PAGED, WIN, WIDE>, C::SMEM, done);
   }
 
-  template <int D, int MT, bool PAGED, bool WIN>
+  template <int D, int MT, bool PAGED, bool WIN, bool WIDE>
   static cudaError_t run(const AttnArgs& a, cudaStream_t st) {
     using C = AttnCfg<D, MT>;
-    cudaError_t e = prepare<D, MT, PAGED, WIN>();
+    cudaError_t e = prepare<D, MT, PAGED, WIN, WIDE>();
     if (e != cudaSuccess) return e;
     const long long blocks = (long long)a.b * a.hkv * a.row_blocks;
-    e = launch_pdl(verify_attn_kernel<D, MT, PAGED, WIN>,
+    e = launch_pdl(verify_attn_kernel<D, MT, PAGED, WIN, WIDE>,
                    dim3((unsigned)(blocks * a.splits)), dim3(C::NT), C::SMEM, st, a);
     if (e != cudaSuccess) return e;
     note_launches(1);
@@ -53,19 +53,22 @@ struct AttnHost {
     return cudaSuccess;
   }
 
-  template <int D, bool PAGED, bool WIN>
+  template <int D, bool PAGED, bool WIN, bool WIDE>
   static cudaError_t by_mt(const AttnArgs& a, int mt, cudaStream_t st) {
     switch (mt) {
-      case 1: return run<D, 1, PAGED, WIN>(a, st);
-      case 2: return run<D, 2, PAGED, WIN>(a, st);
-      case 3: return run<D, 3, PAGED, WIN>(a, st);
-      default: return run<D, 4, PAGED, WIN>(a, st);
+      case 1: return run<D, 1, PAGED, WIN, WIDE>(a, st);
+      case 2: return run<D, 2, PAGED, WIN, WIDE>(a, st);
+      case 3: return run<D, 3, PAGED, WIN, WIDE>(a, st);
+      default: return run<D, 4, PAGED, WIN, WIDE>(a, st);
     }
   }
 
+  // The window variant always uses the 64-bit table (the host splits).
   template <int D, bool PAGED>
   static cudaError_t by_win(const AttnArgs& a, int mt, cudaStream_t st) {
-    return a.has_win ? by_mt<D, PAGED, true>(a, mt, st) : by_mt<D, PAGED, false>(a, mt, st);
+    if (a.has_win) return by_mt<D, PAGED, true, false>(a, mt, st);
+    return a.wide ? by_mt<D, PAGED, false, true>(a, mt, st)
+                  : by_mt<D, PAGED, false, false>(a, mt, st);
   }
 
   static cudaError_t launch(const AttnArgs& a, int d, int mt, bool paged,
@@ -76,10 +79,10 @@ struct AttnHost {
 
   template <int D, int MT>
   static int occ() {
-    if (prepare<D, MT, false, false>() != cudaSuccess) return 1;
+    if (prepare<D, MT, false, false, false>() != cudaSuccess) return 1;
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &n, verify_attn_kernel<D, MT, false, false>, AttnCfg<D, MT>::NT,
+            &n, verify_attn_kernel<D, MT, false, false, false>, AttnCfg<D, MT>::NT,
             AttnCfg<D, MT>::SMEM) != cudaSuccess)
       return 1;
     return n > 0 ? n : 1;

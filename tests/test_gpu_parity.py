@@ -43,6 +43,10 @@ SHAPES = [
     (4, 14, 2, 64, 4, 129, 65),
     (48, 32, 8, 128, 2, 600, 300),
     (40, 16, 4, 64, 3, 400, 130),
+    # k past 4096 with enough units for one CTA each: one row table of
+    # 5000 positions per CTA (d 128) and 7000 (d 64, two row tiles)
+    (16, 16, 8, 128, 2, 6000, 5000),
+    (12, 56, 8, 64, 4, 7500, 7000),
 ]
 
 
@@ -58,7 +62,7 @@ def test_sparse_attention_parity(shape):
     H.assert_attn_close(o, lse, o_ref, lse_ref)
 
 
-DENSE_SHAPES = SHAPES[:6] + SHAPES[8:]
+DENSE_SHAPES = SHAPES[:6] + SHAPES[8:10]
 
 
 @pytest.mark.parametrize("shape", DENSE_SHAPES, ids=[str(s) for s in DENSE_SHAPES])
@@ -156,7 +160,7 @@ def test_kv_ready_launch_overlap_gives_identical_results(case):
 # ------------------------------------------- window causal block merged in
 
 WINDOW_SHAPES = [SHAPES[0], SHAPES[2], SHAPES[4], SHAPES[6], SHAPES[9],
-                 (2, 16, 2, 128, 4, 40, 0)]
+                 (2, 16, 2, 128, 4, 40, 0), SHAPES[10]]
 
 
 @pytest.mark.parametrize("shape", WINDOW_SHAPES, ids=[str(s) for s in WINDOW_SHAPES])
@@ -333,9 +337,12 @@ def test_sparse_with_all_positions_matches_full():
     assert (l1 - l2).abs().max().item() <= 1e-4
 
 
-@pytest.mark.parametrize("page", [16, 32])
-def test_paged_layout_matches_contiguous_and_oracle(page):
-    b, hq, hkv, d, w, n, k = 2, 16, 2, 128, 4, 1000, 300
+@pytest.mark.parametrize("page,shape", [(16, (2, 16, 2, 128, 4, 1000, 300)),
+                                        (32, (2, 16, 2, 128, 4, 1000, 300)),
+                                        (16, (16, 16, 8, 128, 2, 6000, 5000))],
+                         ids=["p16", "p32", "p16-k5000"])
+def test_paged_layout_matches_contiguous_and_oracle(page, shape):
+    b, hq, hkv, d, w, n, k = shape
     q, kk, v = qkv(b, hq, hkv, d, w, n, seed=page)
     pk, pv, table = I.to_paged(kk, v, page, seed=page + 1)
     idx = I.random_sorted_indices(b, n, k, seed=3).to(DEV)

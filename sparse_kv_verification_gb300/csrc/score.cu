@@ -12,7 +12,8 @@
 // workspace and keeps an online (max, sum of 2^(l - max)) per row.
 // Pass 2 (score_reduce_kernel): combines the chunk statistics into each
 // row's log2-sum-exp and writes S[b][j] = sum_{p,r} 2^(l - lse2), summed
-// in a fixed order (pair-major, then row) in fp32.
+// in a fixed order (pair-major, then row) in fp32, four positions per
+// thread with the logits loads batched ahead of the sums.
 #include <cuda.h>
 
 #include <algorithm>
@@ -212,13 +213,46 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// One thread per 4 consecutive positions j of one sequence (16-byte loads
+// when n % 4 == 0, 16-byte stores when S is 16-byte aligned too), 1024 per
+// CTA.  The logits of the first kReduceRows rows
+// are requested before the row statistics are combined, so their latency
+// overlaps that step; later rows follow in batches of the same size, every
+// batch's loads issued before any of its sums.  S is summed per position in
+// row order, as a single chain.
+constexpr int kReduceRows = 8;
+
 __global__ void __launch_bounds__(256) score_reduce_kernel(const ScoreArgs a) {
   __shared__ float lse2[1024];
   const int bb = blockIdx.y;
   const int prs = a.n_pairs * a.rows;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const long long j0 = (long long)blockIdx.x * 1024 + threadIdx.x * 4;
+  const bool vec = (a.n & 3) == 0;   // logits rows start 16-byte aligned
+  const bool vec_out = vec && (reinterpret_cast<uintptr_t>(a.s_out) & 15u) == 0;
   griddep_wait();
   griddep_launch_dependents();
+
+  auto load_batch = [&](int i0, float4 (&v)[kReduceRows]) {
+#pragma unroll
+    for (int u = 0; u < kReduceRows; ++u) {
+      const int i = i0 + u;
+      v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i >= prs || j0 >= a.n) continue;
+      const float* row = a.logits + ((long long)i * a.b + bb) * a.n;
+      if (vec) {
+        v[u] = __ldg(reinterpret_cast<const float4*>(row + j0));
+      } else {
+        v[u].x = __ldg(row + j0);
+        if (j0 + 1 < a.n) v[u].y = __ldg(row + j0 + 1);
+        if (j0 + 2 < a.n) v[u].z = __ldg(row + j0 + 2);
+        if (j0 + 3 < a.n) v[u].w = __ldg(row + j0 + 3);
+      }
+    }
+  };
+  float4 v[kReduceRows];
+  load_batch(0, v);
+
   // Row i's log2-sum-exp from its chunk statistics: one warp per row, the
   // lanes over the chunks.
   for (int i = warp; i < prs; i += 8) {
@@ -236,15 +270,29 @@ __global__ void __launch_bounds__(256) score_reduce_kernel(const ScoreArgs a) {
     if (lane == 0) lse2[i] = Z > 0.f ? u + log2f(Z) : INFINITY;
   }
   __syncthreads();
-  const long long base = (long long)blockIdx.x * 1024;
+
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i0 = 0; i0 < prs; i0 += kReduceRows) {
+    if (i0 > 0) load_batch(i0, v);
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const long long j = base + q * 256 + threadIdx.x;
-    if (j >= a.n) continue;
-    float acc = 0.f;
-    for (int i = 0; i < prs; ++i)
-      acc += ex2(a.logits[((long long)i * a.b + bb) * a.n + j] - lse2[i]);
-    a.s_out[(long long)bb * a.n + j] = acc;
+    for (int u = 0; u < kReduceRows; ++u) {
+      if (i0 + u >= prs) break;
+      const float L = lse2[i0 + u];
+      acc.x += ex2(v[u].x - L);
+      acc.y += ex2(v[u].y - L);
+      acc.z += ex2(v[u].z - L);
+      acc.w += ex2(v[u].w - L);
+    }
+  }
+  if (j0 >= a.n) return;
+  float* out = a.s_out + (long long)bb * a.n;
+  if (vec_out) {
+    *reinterpret_cast<float4*>(out + j0) = acc;
+  } else {
+    out[j0] = acc.x;
+    if (j0 + 1 < a.n) out[j0 + 1] = acc.y;
+    if (j0 + 2 < a.n) out[j0 + 2] = acc.z;
+    if (j0 + 3 < a.n) out[j0 + 3] = acc.w;
   }
 }
 

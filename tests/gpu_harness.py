@@ -79,14 +79,15 @@ def full_attn_window(q, k, v, kw, vw, scale, n=None, page_table=None, flags=0):
     return o, lse
 
 
-def score(q, keys, kv_heads, scale, n, page_tables=None):
-    """q [P][b][rows][d]; keys: list of K tensors (one per pair)."""
+def score(q, keys, kv_heads, scale, n, page_tables=None, out=None):
+    """q [P][b][rows][d]; keys: list of K tensors (one per pair); out: an
+    optional [b][n] fp32 output (any 4-byte alignment)."""
     p, b, rows, d = q.shape
     pts = page_tables or [None] * p
     descs = [N.kv_desc(k, None, pt) for k, pt in zip(keys, pts)]
     ws = N.workspace(N.dustin_score_heads_workspace_size(b, n, p, rows),
                      q.device)
-    s = torch.full((b, n), float("nan"), device=q.device)
+    s = torch.full((b, n), float("nan"), device=q.device) if out is None else out
     N.dustin_score_heads(q, descs, kv_heads, scale, s, ws, n)
     sync()
     return s

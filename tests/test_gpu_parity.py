@@ -429,6 +429,20 @@ def test_score_heads_paged_matches_contiguous():
     assert torch.equal(s_c, s_p)
 
 
+def test_score_heads_unaligned_output():
+    """S at an address that is 4- but not 16-byte aligned: the same bits."""
+    p, b, rows, d, n = 2, 3, 5, 64, 2048
+    g = I.generator(91)
+    q = torch.randn((p, b, rows, d), generator=g).to(torch.bfloat16).to(DEV)
+    keys = [torch.randn((b, 2, n, d), generator=g).to(torch.bfloat16).to(DEV)
+            for _ in range(p)]
+    s_a = H.score(q, keys, [0, 1], 0.125, n)
+    buf = torch.full((b * n + 4,), float("nan"), device=DEV)
+    s_u = H.score(q, keys, [0, 1], 0.125, n, out=buf[1:1 + b * n].view(b, n))
+    assert torch.equal(s_a, s_u)
+    assert torch.isnan(buf[0]) and torch.isnan(buf[1 + b * n:]).all()
+
+
 # ---------------------------------------------------------------- selection
 
 SELECT_CASES = [

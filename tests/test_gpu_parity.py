@@ -467,6 +467,10 @@ SELECT_CASES = [
     (2, 12345, 1500, 3, 17, 0.3, -1, 1, True),
     (1, 400000, 4000, 4, 64, 0.5, -1, 1, False),
     (1, 400000, 4000, 4, 64, 0.5, 1000, 1, False),
+    # 16 sequences: 8-CTA clusters do not all fit at once, so each sequence
+    # gets a smaller cluster
+    (16, 32768, 2048, 4, 64, 0.5, -1, 1, True),
+    (16, 20000, 3000, 2, 8, 0.7, 600, 1, True),
 ]
 
 

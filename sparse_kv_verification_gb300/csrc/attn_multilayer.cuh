@@ -172,6 +172,7 @@ __global__ void __launch_bounds__(SkCfg<D, MT>::NT, 1)
         __syncwarp();
       }
       const __nv_bfloat16* src_base = is_v ? Ld.kv.v : Ld.kv.k;
+      const uint64_t pol = policy_evict_first();   // K/V rows are read once
       // The kv heads of a sequence share idx: start head g at tile
       // g tpu / hkv so that they do not read the same positions together.
       const int rot = DUSTIN_ATTN_ROTATE ? (int)(((long long)x.g * a.tpu) / a.hkv) : 0;
@@ -195,8 +196,8 @@ __global__ void __launch_bounds__(SkCfg<D, MT>::NT, 1)
           const int rr = q * RPI + sub;             // row within this warp's rows
           const long long off = __shfl_sync(0xffffffffu, my_off, rr);
           const bool ok = off >= 0;
-          cp_async_16(smem_u32(dst + (pw * C::RPW + rr) * C::RS),
-                      src_base + (ok ? off + ch * 8 : 0), ok ? 16 : 0);
+          cp_async_16_hint(smem_u32(dst + (pw * C::RPW + rr) * C::RS),
+                           src_base + (ok ? off + ch * 8 : 0), ok ? 16 : 0, pol);
         }
         cp_async_mbar_arrive(full_bar(st));
         if (lane == 0) {

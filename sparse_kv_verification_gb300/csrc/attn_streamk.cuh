@@ -357,6 +357,7 @@ __global__ void __launch_bounds__(SkCfg<D, MT>::NT, 1)
         load_q(u, pw * 32 + lane, C::NPW * 32);
         cp_async_mbar_arrive(q_full);
       }
+      const uint64_t pol = policy_evict_first();   // K/V are read once
       for (int lt = lt0; lt < lt1; ++lt, ++t) {
         const int st = t % C::STAGES;
         if (t >= C::STAGES) ensure_wait();
@@ -393,8 +394,8 @@ __global__ void __launch_bounds__(SkCfg<D, MT>::NT, 1)
           const int rr = it * RPI + sub;            // row within this warp's rows
           const long long off = __shfl_sync(0xffffffffu, my_off, rr);
           const bool ok = off >= 0;
-          cp_async_16(smem_u32(dst + (pw * C::RPW + rr) * C::RS),
-                      src + (ok ? off + ch * 8 : 0), ok ? 16 : 0);
+          cp_async_16_hint(smem_u32(dst + (pw * C::RPW + rr) * C::RS),
+                           src + (ok ? off + ch * 8 : 0), ok ? 16 : 0, pol);
         }
         cp_async_mbar_arrive(full_bar(st));
         if (lane == 0) {

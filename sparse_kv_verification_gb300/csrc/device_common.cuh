@@ -34,6 +34,12 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src,
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst),
                "l"(src), "r"(src_bytes));
 }
+// The same under an L2 cache policy (see policy_evict_first).
+__device__ __forceinline__ void cp_async_16_hint(uint32_t dst, const void* src,
+                                                 int src_bytes, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;\n" ::"r"(dst),
+               "l"(src), "r"(src_bytes), "l"(policy));
+}
 // 16-byte global -> shared copy, no zero-fill operand.
 __device__ __forceinline__ void cp_async_16_full(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src));
@@ -145,15 +151,23 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src,
 }
 // Tiled TMA load of a 3-D box (coordinates in elements, innermost first)
 // through the tensor map at `map` (a __grid_constant__ kernel parameter),
-// completing on `bar`.  The innermost coordinate times the element size
-// must be a multiple of 16 bytes.
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, int x, int y,
-                                            int z, uint32_t bar) {
+// completing on `bar`, under the L2 cache policy `policy` (policy_evict_first
+// below: for streams read once, so that they do not push out lines that are
+// read again soon).  The innermost coordinate times the element size must
+// be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void* map, int x, int y,
+                                                 int z, uint32_t bar, uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
       : "memory");
+}
+// L2 policy: lines fetched under it are the first candidates for eviction.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(p));
+  return p;
 }
 // Arrives on `bar` once every cp.async this thread issued so far has landed
 // (the barrier's expected count includes this arrival).

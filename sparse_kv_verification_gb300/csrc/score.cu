@@ -399,6 +399,9 @@ __global__ void __launch_bounds__(TmaCfg<D>::NT)
       }
       cp_async_mbar_arrive(q_full);
       const void* map = &ta.maps[x.p];
+      // Keys are read once: evict them first, so the logits written
+      // meanwhile are still in L2 when the second pass reads them.
+      const uint64_t pol = policy_evict_first();
       for (int tt = 0; tt < tpi; ++tt, ++t) {
         const int st = t % T::STAGES;
         if (t >= T::STAGES &&
@@ -413,7 +416,8 @@ __global__ void __launch_bounds__(TmaCfg<D>::NT)
           const int j0 = x.c * a.chunk + tt * kTile;
 #pragma unroll
           for (int h = 0; h < T::HALVES; ++h)
-            tma_load_3d(dst + h * (kTile * 128), map, h * 64, j0, x.bb, full_bar(st));
+            tma_load_3d_hint(dst + h * (kTile * 128), map, h * 64, j0, x.bb, full_bar(st),
+                             pol);
         }
         __syncwarp();
       }

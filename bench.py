@@ -712,7 +712,7 @@ def run_ours(args):
                  "speedup_step": t_dense * L / 1e3 / t_ms}
 
     # ---- end to end: queries from pinned host memory in, outputs out.
-    # Copies run on two copy streams beside the compute stream, in 16 chunks
+    # Copies run on two copy streams beside the compute stream, in chunks
     # of layers: the scoring queries and the first layers' queries go in
     # first, each chunk's attention waits only for its own queries, and
     # each chunk's outputs go out as soon as they are written.  A step waits
@@ -722,8 +722,20 @@ def run_ours(args):
     if not args.no_e2e:
         inp = rep.inp
         L = rep.L
-        n_chunks = min(16, L)
-        bounds = [L * c // n_chunks for c in range(n_chunks + 1)]
+        # Chunks of up to 6 layers, shrinking to 4, 2, 1, 1 layers at the
+        # end, so that little output is left to copy after the last kernel.
+        tail = []
+        for size in (1, 1, 2, 4):
+            if sum(tail) + size <= L // 2:
+                tail.insert(0, size)
+        head = L - sum(tail)
+        n_head = -(-head // 6) if head else 0
+        sizes = [head * (c + 1) // n_head - head * c // n_head
+                 for c in range(n_head)] + tail
+        bounds = [0]
+        for size in sizes:
+            bounds.append(bounds[-1] + size)
+        n_chunks = len(sizes)
         h_qt, h_qd = inp.q_t.cpu().pin_memory(), inp.q_d.cpu().pin_memory()
         h_q = rep.q_all.cpu().pin_memory()
         h_o = torch.empty(rep.o_all.shape, dtype=rep.o_all.dtype, pin_memory=True)

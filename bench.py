@@ -383,22 +383,24 @@ def run_extras(rep, wl, dev, stream, L, args, t_attn, t_dense):
 # ----------------------------------------------------------------- sweep
 
 def run_sweep(args):
-    """The 72B-shape sweep: for n in 4K..64K and b in {1, 16}, the step's
-    scoring (target + draft) and select, and per layer the sparse attention
-    for each budget k and the dense attention.  Layer buffers are cycled so
-    that each pass reads well past L2.  Crossover (amortised over 80 layers):
-    the smallest tested k/n at which scoring + select + 80 sparse layers
-    take at least as long as 80 dense layers.  One JSON line per (n, b),
-    then a summary line."""
+    """The 72B-shape sweep on paged caches (page 16, seeded random page
+    tables): for n in 4K..64K and b in {1, 4, 16, 32} (w = 4, 8 scored
+    pairs), the step's scoring (target + draft) and select, and per layer
+    the sparse attention for each budget k and the dense attention; then
+    w in {2, 4, 8} and scored pairs in {1, 4, 8, 16} at n = 32K, b = 16,
+    k = 2048, and the contiguous cache at that point.  Layer buffers are
+    cycled so that each pass reads well past L2.  Crossover (amortised over
+    80 layers): the smallest tested k/n at which scoring + select + 80
+    sparse layers take at least as long as 80 dense layers.  One JSON line
+    per point, then a summary line."""
     import torch
     from sparse_kv_verification_gb300 import build, inputs as I, native as N
     build.build()
     N.load()
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    w, pairs, layers_model = 5, 8, 80
+    layers_model, page = 80, 16
     ks_all = [256, 512, 1024, 2048, 4096, 8192]
-    out = []
 
     def timed(calls, reps):
         for c in calls:
@@ -413,97 +415,110 @@ def run_sweep(args):
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) * 1e3 / (reps * len(calls))
 
-    for n in (4096, 8192, 16384, 32768, 65536):
-        for b in (1, 16):
-            ks = [k for k in ks_all if k < n]
-            wl = I.sweep_workload(n, b, w, max(ks), pairs)
-            layer_bytes = b * wl.hkv * n * wl.d * 2 * 2
-            n_buf = int(min(layers_model, max(3, -(-400_000_000 // layer_bytes))))
-            inp = I.step_inputs(wl, dev, n_buf)
-            s_t = torch.empty((b, n), device=dev)
-            s_d = torch.empty((b, n), device=dev)
-            ws_t = N.workspace(N.dustin_score_heads_workspace_size(b, n, wl.p_t, 1), dev)
-            ws_d = N.workspace(N.dustin_score_heads_workspace_size(b, n, wl.p_d, wl.gamma), dev)
-            sc_t = N.prepare_score_heads(inp.q_t, [N.kv_desc(k) for k in inp.k_t],
-                                         inp.kvh_t, wl.scale, s_t, ws_t, n)
-            sc_d = N.prepare_score_heads(inp.q_d, [N.kv_desc(k) for k in inp.k_d],
-                                         inp.kvh_d, wl.draft_scale, s_d, ws_d, n)
-            t_score = timed([sc_t], 5) + timed([sc_d], 5)
+    def point(n, b, w, pairs, ks, paged=True):
+        wl = I.sweep_workload(n, b, w, max(ks), pairs)
+        layer_bytes = b * wl.hkv * n * wl.d * 2 * 2
+        n_buf = int(min(layers_model, max(3, -(-400_000_000 // layer_bytes))))
+        inp = I.step_inputs(wl, dev, n_buf)
+        if paged:
+            kt = [I.to_paged(k, None, page, seed=100 + i) for i, k in enumerate(inp.k_t)]
+            kd = [I.to_paged(k, None, page, seed=200 + i) for i, k in enumerate(inp.k_d)]
+            desc_t = [N.kv_desc(pk, None, t) for pk, _, t in kt]
+            desc_d = [N.kv_desc(pk, None, t) for pk, _, t in kd]
+            kvp = []
+            for l in range(n_buf):
+                kvp.append(I.to_paged(inp.k[l], inp.v[l], page, seed=300 + l))
+                inp.k[l] = inp.v[l] = None   # keep only the paged copy
+            kvs = [N.kv_desc(pk, pv, t) for pk, pv, t in kvp]
+        else:
+            kt = kd = kvp = None
+            desc_t = [N.kv_desc(k) for k in inp.k_t]
+            desc_d = [N.kv_desc(k) for k in inp.k_d]
             kvs = [N.kv_desc(k, v) for k, v in zip(inp.k, inp.v)]
-            o = [torch.empty_like(q) for q in inp.q]
-            lse = [torch.empty(q.shape[:3], device=dev) for q in inp.q]
-            ws_f = N.workspace(N.dustin_full_verify_attn_workspace_size(
-                b, wl.hq, wl.hkv, wl.d, w, n), dev)
-            ready = lambda l: N.DUSTIN_ATTN_KV_READY if l > 0 else 0
-            dense = [N.prepare_full_verify_attn(inp.q[l], kvs[l], wl.hkv, n, wl.scale, o[l],
-                                                lse[l], ws_f, flags=ready(l))
-                     for l in range(n_buf)]
-            t_dense = timed(dense, max(1, 6 // n_buf + 1))
-            points = []
-            for k in ks:
-                idx = torch.empty((b, k), dtype=torch.int32, device=dev)
-                sel = N.prepare_hybrid_topk(s_d, s_t, k, wl.n_sink, wl.n_recent, wl.alpha,
-                                            wl.m, N.DUSTIN_NORM_L1, idx)
-                t_sel = timed([sel], 5)
-                ws_a = N.workspace(N.dustin_sparse_verify_attn_workspace_size(
-                    b, wl.hq, wl.hkv, wl.d, w, k), dev)
-                sparse = [N.prepare_sparse_verify_attn(inp.q[l], kvs[l], wl.hkv, n, idx,
-                                                       wl.scale, o[l], lse[l], ws_a,
-                                                       flags=ready(l))
-                          for l in range(n_buf)]
-                t_sp = timed(sparse, max(1, 30 // n_buf + 1))
-                est = t_score + t_sel
-                points.append({
-                    "k": k, "k_over_n": k / n, "select_us": t_sel, "sparse_us_per_layer": t_sp,
-                    "speedup_attention_per_layer": t_dense / t_sp,
-                    "speedup_amortised_80": layers_model * t_dense /
-                                            (est + layers_model * t_sp),
-                    "speedup_estimation_charged_to_one_layer": t_dense / (est + t_sp),
-                })
-            cross = next((p["k_over_n"] for p in points if p["speedup_amortised_80"] <= 1.0),
-                         None)
-            cross1 = next((p["k_over_n"] for p in points
-                           if p["speedup_estimation_charged_to_one_layer"] <= 1.0), None)
-            line = {"sweep": True, "n": n, "b": b, "w": w, "pairs": pairs,
-                    "layer_buffers": n_buf, "score_us": t_score,
-                    "dense_us_per_layer": t_dense, "points": points,
-                    "crossover_k_over_n_amortised": cross,
-                    "crossover_k_over_n_charged_to_one_layer": cross1}
-            print(json.dumps(line), flush=True)
-            out.append(line)
-            del inp, kvs, o, lse, dense, sparse
-            torch.cuda.empty_cache()
-    # The paged cache at the headline point.
-    wl = I.sweep_workload(32768, 16, w, 2048, pairs)
-    inp = I.step_inputs(wl, dev, 3)
-    idx = I.random_sorted_indices(wl.b, wl.n, wl.k, seed=7).to(dev)
-    ws_a = N.workspace(N.dustin_sparse_verify_attn_workspace_size(
-        wl.b, wl.hq, wl.hkv, wl.d, w, wl.k), dev)
-    t_c, t_p = [], []
-    for l in range(3):
-        o = torch.empty_like(inp.q[l])
-        ls = torch.empty(inp.q[l].shape[:3], device=dev)
-        c = N.prepare_sparse_verify_attn(inp.q[l], N.kv_desc(inp.k[l], inp.v[l]), wl.hkv,
-                                         wl.n, idx, wl.scale, o, ls, ws_a)
-        t_c.append(timed([c], 20))
-        pk, pv, table = I.to_paged(inp.k[l], inp.v[l], 16, seed=l)
-        pc = N.prepare_sparse_verify_attn(inp.q[l], N.kv_desc(pk, pv, table), wl.hkv, wl.n,
-                                          idx, wl.scale, o, ls, ws_a)
-        t_p.append(timed([pc], 20))
-        del pk, pv, table
+        s_t = torch.empty((b, n), device=dev)
+        s_d = torch.empty((b, n), device=dev)
+        ws_t = N.workspace(N.dustin_score_heads_workspace_size(b, n, wl.p_t, 1), dev)
+        ws_d = N.workspace(N.dustin_score_heads_workspace_size(b, n, max(1, wl.p_d),
+                                                                wl.gamma), dev)
+        sc_t = N.prepare_score_heads(inp.q_t, desc_t, inp.kvh_t, wl.scale, s_t, ws_t, n)
+        t_score = timed([sc_t], 5)
+        alpha = wl.alpha
+        if wl.p_d > 0:
+            sc_d = N.prepare_score_heads(inp.q_d, desc_d, inp.kvh_d, wl.draft_scale, s_d,
+                                         ws_d, n)
+            t_score += timed([sc_d], 5)
+        else:   # a single scored pair: the target's, selected on its own
+            s_d, alpha = None, 0.0
+        o = [torch.empty_like(q) for q in inp.q]
+        lse = [torch.empty(q.shape[:3], device=dev) for q in inp.q]
+        ws_f = N.workspace(N.dustin_full_verify_attn_workspace_size(
+            b, wl.hq, wl.hkv, wl.d, w, n), dev)
+        ready = lambda l: N.DUSTIN_ATTN_KV_READY if l > 0 else 0
+        dense = [N.prepare_full_verify_attn(inp.q[l], kvs[l], wl.hkv, n, wl.scale, o[l],
+                                            lse[l], ws_f, flags=ready(l))
+                 for l in range(n_buf)]
+        t_dense = timed(dense, max(1, 6 // n_buf + 1))
+        points = []
+        for k in ks:
+            idx = torch.empty((b, k), dtype=torch.int32, device=dev)
+            sel = N.prepare_hybrid_topk(s_d, s_t, k, wl.n_sink, wl.n_recent, alpha,
+                                        wl.m, N.DUSTIN_NORM_L1, idx)
+            t_sel = timed([sel], 5)
+            ws_a = N.workspace(N.dustin_sparse_verify_attn_workspace_size(
+                b, wl.hq, wl.hkv, wl.d, w, k), dev)
+            sparse = [N.prepare_sparse_verify_attn(inp.q[l], kvs[l], wl.hkv, n, idx,
+                                                   wl.scale, o[l], lse[l], ws_a,
+                                                   flags=ready(l))
+                      for l in range(n_buf)]
+            t_sp = timed(sparse, max(1, 30 // n_buf + 1))
+            est = t_score + t_sel
+            points.append({
+                "k": k, "k_over_n": k / n, "select_us": t_sel, "sparse_us_per_layer": t_sp,
+                "speedup_attention_per_layer": t_dense / t_sp,
+                "speedup_amortised_80": layers_model * t_dense /
+                                        (est + layers_model * t_sp),
+                "speedup_estimation_charged_to_one_layer": t_dense / (est + t_sp),
+            })
+        cross = next((p["k_over_n"] for p in points if p["speedup_amortised_80"] <= 1.0),
+                     None)
+        cross1 = next((p["k_over_n"] for p in points
+                       if p["speedup_estimation_charged_to_one_layer"] <= 1.0), None)
+        line = {"sweep": True, "n": n, "b": b, "w": w, "pairs": pairs,
+                "kv": f"paged{page}" if paged else "contiguous",
+                "layer_buffers": n_buf, "score_us": t_score,
+                "dense_us_per_layer": t_dense, "points": points,
+                "crossover_k_over_n_amortised": cross,
+                "crossover_k_over_n_charged_to_one_layer": cross1}
+        print(json.dumps(line), flush=True)
+        del inp, kvs, o, lse, dense, sparse, kt, kd, kvp, desc_t, desc_d
+        torch.cuda.empty_cache()
+        return line
+
+    grid = []
+    for n in (4096, 8192, 16384, 32768, 65536):
+        for b in (1, 4, 16, 32):
+            grid.append(point(n, b, 4, 8, [k for k in ks_all if k < n]))
+    by_w = [point(32768, 16, w, 8, [2048]) for w in (2, 4, 8)]
+    by_pairs = [point(32768, 16, 4, p, [2048]) for p in (1, 4, 8, 16)]
+    contiguous = point(32768, 16, 4, 8, [2048], paged=False)
+    key = lambda l: f"n{l['n']}_b{l['b']}"
     summary = {"sweep_summary": True,
-               "crossovers_amortised_80": {f"n{l['n']}_b{l['b']}":
-                                           l["crossover_k_over_n_amortised"] for l in out},
+               "crossovers_amortised_80": {key(l): l["crossover_k_over_n_amortised"]
+                                           for l in grid},
                "crossovers_charged_to_one_layer": {
-                   f"n{l['n']}_b{l['b']}": l["crossover_k_over_n_charged_to_one_layer"]
-                   for l in out},
+                   key(l): l["crossover_k_over_n_charged_to_one_layer"] for l in grid},
+               "sparse_us_by_w": {l["w"]: l["points"][0]["sparse_us_per_layer"]
+                                  for l in by_w},
+               "score_us_by_pairs": {l["pairs"]: l["score_us"] for l in by_pairs},
                "paged16_vs_contiguous_sparse_us": {
-                   "contiguous": statistics.median(t_c), "paged": statistics.median(t_p)}}
+                   "paged": by_w[1]["points"][0]["sparse_us_per_layer"],
+                   "contiguous": contiguous["points"][0]["sparse_us_per_layer"]},
+               "paged16_vs_contiguous_dense_us": {
+                   "paged": by_w[1]["dense_us_per_layer"],
+                   "contiguous": contiguous["dense_us_per_layer"]}}
     print(json.dumps(summary), flush=True)
     return 0
 
-
-# ----------------------------------------------------------------- oracle leg
 
 def oracle_worker(args):
     """Runs inside a fresh single-threaded process: the CPU oracle on a

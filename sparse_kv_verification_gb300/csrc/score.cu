@@ -307,9 +307,16 @@ __global__ void __launch_bounds__(256) score_reduce_kernel(const ScoreArgs a) {
 // past n come back as zeros.  Four consumer warps take 16 positions each per
 // tile, as in the cp.async kernel, and release the stage through its
 // "empty" mbarrier.  Every wait is bounded and raises flag 0x4 on timeout.
+// Paged caches (page size 16, 32 or 64): the tensor map of a pair views its
+// kv head of the page pool as [P][page][d], and a tile is 64 / page boxes of
+// one page each, whose ids the producer lanes read from the page table once
+// per item (one page per lane); a page id outside the pool raises flag 0x2,
+// its box is filled with zeros (an out-of-range coordinate) and its rows
+// are left out through a per-stage mask, as in the cp.async kernel.
 struct ScoreTmaArgs {
   ScoreArgs s;
   CUtensorMap maps[kMaxPairs];   // per pair: kv head kv_head as [b][n][d]
+                                 // (paged: [P][page][d])
 };
 
 // Build-time tunables: TMA pipeline depth per CTA (several CTAs share an
@@ -331,11 +338,12 @@ struct TmaCfg {
   static constexpr int OFF_RED = OFF_Q + Q_BYTES;
   static constexpr int OFF_BAR = OFF_RED + kWarps * 16 * 8;
   static constexpr int NBARS = 2 * STAGES + 2;
-  static constexpr int SMEM = OFF_BAR + NBARS * 8 + 1024;    // + alignment slack
+  static constexpr int OFF_BAD = OFF_BAR + NBARS * 8;        // paged: bad-page mask / stage
+  static constexpr int SMEM = OFF_BAD + STAGES * 4 + 1024;   // + alignment slack
   static constexpr int NT = (kWarps + 1) * 32;
 };
 
-template <int D>
+template <int D, bool PAGED>
 __global__ void __launch_bounds__(TmaCfg<D>::NT)
     score_logits_tma_kernel(const __grid_constant__ ScoreTmaArgs ta) {
   using C = ScoreCfg<D>;
@@ -352,6 +360,7 @@ __global__ void __launch_bounds__(TmaCfg<D>::NT)
   auto empty_bar = [&](int s) { return bar0 + 8u * (T::STAGES + s); };
   const uint32_t q_full = bar0 + 8u * (2 * T::STAGES);
   const uint32_t q_empty = q_full + 8u;
+  unsigned* sBad = reinterpret_cast<unsigned*>(smem + T::OFF_BAD);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int tpi = a.chunk / kTile;
@@ -399,6 +408,28 @@ __global__ void __launch_bounds__(TmaCfg<D>::NT)
       }
       cp_async_mbar_arrive(q_full);
       const void* map = &ta.maps[x.p];
+      // Paged: lane l holds the pool page of the chunk's l-th page (-1: past
+      // n, or failed its check: read as zeros at an out-of-range page).
+      int my_pid = -1;
+      unsigned bad_pages = 0;
+      int ps = kTile, pool = 0;
+      if constexpr (PAGED) {
+        const KvView& kv = a.pairs[x.p].kv;
+        ps = kv.page_size;
+        pool = kv.num_pages;
+        const int pi = x.c * (a.chunk / ps) + lane;
+        bool bad = false;
+        if (lane < a.chunk / ps && (long long)pi * ps < a.n) {
+          const int pid = __ldg(kv.page_table + (long long)x.bb * kv.pages_per_seq + pi);
+          if (pid < 0 || pid >= kv.num_pages) {
+            bad = true;
+            atomicOr(&g_score_dev_flags, 2u);
+          } else {
+            my_pid = pid;
+          }
+        }
+        bad_pages = __ballot_sync(0xffffffffu, bad);
+      }
       // Keys are read once: evict them first, so the logits written
       // meanwhile are still in L2 when the second pass reads them.
       const uint64_t pol = policy_evict_first();
@@ -410,9 +441,23 @@ __global__ void __launch_bounds__(TmaCfg<D>::NT)
           ok_run = false;
           break;
         }
-        if (lane == 0) {
+        const uint32_t dst = smem_u32(smem + st * T::TILE_BYTES);
+        if constexpr (PAGED) {
+          const int ppt = kTile / ps;   // pages per tile
+          const int pid = __shfl_sync(0xffffffffu, my_pid, tt * ppt + lane % ppt);
+          if (lane == 0) {
+            sBad[st] = (bad_pages >> (tt * ppt)) & ((1u << ppt) - 1u);
+            mbar_arrive_expect_tx(full_bar(st), T::TILE_BYTES);
+          }
+          __syncwarp();
+          if (lane < ppt) {
+#pragma unroll
+            for (int h = 0; h < T::HALVES; ++h)
+              tma_load_3d_hint(dst + h * (kTile * 128) + lane * ps * 128, map, h * 64, 0,
+                               pid >= 0 ? pid : pool, full_bar(st), pol);
+          }
+        } else if (lane == 0) {
           mbar_arrive_expect_tx(full_bar(st), T::TILE_BYTES);
-          const uint32_t dst = smem_u32(smem + st * T::TILE_BYTES);
           const int j0 = x.c * a.chunk + tt * kTile;
 #pragma unroll
           for (int h = 0; h < T::HALVES; ++h)
@@ -451,12 +496,15 @@ __global__ void __launch_bounds__(TmaCfg<D>::NT)
     float* outA = a.logits + (((long long)x.p * a.rows + gq) * a.b + x.bb) * a.n;
     float* outB = a.logits + (((long long)x.p * a.rows + gq + 8) * a.b + x.bb) * a.n;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    // Paged: log2 of the page size (16, 32 or 64), for the bad-page mask.
+    const int page_shift = PAGED ? 31 - __clz(a.pairs[x.p].kv.page_size) : 6;
 
     for (int tt = 0; tt < tpi; ++tt, ++t) {
       const int st = t % T::STAGES;
       wait_or_die(full_bar(st), (t / T::STAGES) & 1);
       const unsigned char* tk = smem + st * T::TILE_BYTES;
       const int p0 = x.c * a.chunk + tt * kTile;
+      const unsigned bad = PAGED ? sBad[st] : 0u;   // read before the stage is released
       float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
       const int r = warp * 16 + ((lane >> 4) << 3) + (lane & 7);
 #pragma unroll
@@ -478,13 +526,15 @@ __global__ void __launch_bounds__(TmaCfg<D>::NT)
       for (int jj = 0; jj < 2; ++jj) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const int j = p0 + warp * 16 + jj * 8 + 2 * tq + e;
-          const bool ok = j < a.n;
+          const int pos = warp * 16 + jj * 8 + 2 * tq + e;   // in the tile
+          const int j = p0 + pos;
+          bool ok = j < a.n;
+          if constexpr (PAGED) ok = ok && !((bad >> (pos >> page_shift)) & 1u);
           const float va = ok ? sc[jj][e] * a.scale_log2 : -INFINITY;
           const float vb = ok ? sc[jj][e + 2] * a.scale_log2 : -INFINITY;
           sc[jj][e] = va;
           sc[jj][e + 2] = vb;
-          if (ok) {
+          if (j < a.n) {   // failed page checks store -inf: probability 0
             if (rowA) outA[j] = va;
             if (rowB) outB[j] = vb;
           }
@@ -560,17 +610,24 @@ EncodeTiledFn encode_tiled() {
   return f;
 }
 
-// Tensor maps of every pair; false if one cannot be encoded.
-template <int D>
+// Tensor maps of every pair; false if one cannot be encoded (or, paged, if
+// a page size is not 16, 32 or 64: those pairs go to the cp.async kernel).
+template <int D, bool PAGED>
 bool make_maps(const ScoreArgs& a, ScoreTmaArgs& ta) {
   EncodeTiledFn enc = encode_tiled();
   if (!enc) return false;
   for (int p = 0; p < a.n_pairs; ++p) {
     const KvView& kv = a.pairs[p].kv;
     void* base = const_cast<__nv_bfloat16*>(kv.k + (long long)a.pairs[p].kv_head * kv.sh);
-    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)a.n, (cuuint64_t)a.b};
+    if (PAGED && !(kv.page_size == 16 || kv.page_size == 32 || kv.page_size == 64))
+      return false;
+    // Contiguous: the kv head as [b][n][d], 64-row boxes.  Paged: the kv
+    // head of the pool as [P][page][d], one page a box.
+    const cuuint64_t dims[3] = {(cuuint64_t)D,
+                                (cuuint64_t)(PAGED ? kv.page_size : a.n),
+                                (cuuint64_t)(PAGED ? kv.num_pages : a.b)};
     const cuuint64_t strides[2] = {(cuuint64_t)kv.sn * 2, (cuuint64_t)kv.sb * 2};
-    const cuuint32_t box[3] = {64, (cuuint32_t)kTile, 1};
+    const cuuint32_t box[3] = {64, (cuuint32_t)(PAGED ? kv.page_size : kTile), 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     if (enc(&ta.maps[p], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -581,7 +638,7 @@ bool make_maps(const ScoreArgs& a, ScoreTmaArgs& ta) {
   return true;
 }
 
-template <int D>
+template <int D, bool PAGED>
 cudaError_t run_score_tma(const ScoreArgs& a, cudaStream_t st, bool* used) {
   using T = TmaCfg<D>;
   *used = false;
@@ -589,8 +646,8 @@ cudaError_t run_score_tma(const ScoreArgs& a, cudaStream_t st, bool* used) {
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
   ta.s = a;
-  if (!make_maps<D>(a, ta)) return cudaSuccess;
-  auto kern = score_logits_tma_kernel<D>;
+  if (!make_maps<D, PAGED>(a, ta)) return cudaSuccess;
+  auto kern = score_logits_tma_kernel<D, PAGED>;
   static std::atomic<int> slots_memo[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -622,16 +679,14 @@ cudaError_t run_score_cp(const ScoreArgs& a, cudaStream_t st);
 
 template <int D, bool PAGED>
 cudaError_t run_score(const ScoreArgs& a, cudaStream_t st) {
-  if constexpr (!PAGED) {
-    bool used = false;
-    cudaError_t e = run_score_tma<D>(a, st, &used);
-    if (e != cudaSuccess) return e;
-    if (used) {
-      dim3 g2((unsigned)((a.n + 1023) / 1024), (unsigned)a.b);
-      e = launch_pdl(score_reduce_kernel, g2, dim3(256), 0, st, a);
-      if (e == cudaSuccess) note_launches(1);
-      return e;
-    }
+  bool used = false;
+  cudaError_t e = run_score_tma<D, PAGED>(a, st, &used);
+  if (e != cudaSuccess) return e;
+  if (used) {
+    dim3 g2((unsigned)((a.n + 1023) / 1024), (unsigned)a.b);
+    e = launch_pdl(score_reduce_kernel, g2, dim3(256), 0, st, a);
+    if (e == cudaSuccess) note_launches(1);
+    return e;
   }
   return run_score_cp<D, PAGED>(a, st);
 }

@@ -416,17 +416,46 @@ def test_score_heads_parity(p, b, rows, d, n):
     np.testing.assert_allclose(H.f64(s).sum(axis=1), p * rows, rtol=1e-4)
 
 
-def test_score_heads_paged_matches_contiguous():
-    p, b, rows, d, n = 2, 2, 2, 128, 1500
-    g = I.generator(77)
+@pytest.mark.parametrize("page,d,rows", [(16, 128, 2), (32, 128, 1), (64, 64, 4),
+                                          (16, 64, 5), (48, 128, 2), (128, 64, 3)])
+def test_score_heads_paged_matches_contiguous(page, d, rows):
+    """Paged keys give the contiguous scores bit for bit (page sizes 16, 32
+    and 64 load one page per TMA box; 48 and 128 go to the cp.async
+    kernel)."""
+    p, b, n = 2, 2, 1500
+    g = I.generator(77 + page + d)
     q = torch.randn((p, b, rows, d), generator=g).to(torch.bfloat16).to(DEV)
     keys = [torch.randn((b, 2, n, d), generator=g).to(torch.bfloat16)
             for _ in range(p)]
-    paged = [I.to_paged(k, None, 16, seed=i) for i, k in enumerate(keys)]
+    paged = [I.to_paged(k, None, page, seed=i) for i, k in enumerate(keys)]
     s_c = H.score(q, [k.to(DEV) for k in keys], [0, 1], 0.1, n)
     s_p = H.score(q, [pk.to(DEV) for pk, _, _ in paged], [0, 1], 0.1, n,
                   page_tables=[t.to(DEV) for _, _, t in paged])
     assert torch.equal(s_c, s_p)
+    assert N.dustin_device_status() == 0
+
+
+@pytest.mark.parametrize("page", [16, 48])
+def test_score_heads_bad_page_left_out(page):
+    """A page id outside the pool raises flag 0x2 and its positions are left
+    out: they score 0 and the rest is the softmax over the other positions."""
+    p, b, rows, d, n = 1, 2, 3, 128, 700
+    g = I.generator(500 + page)
+    q = torch.randn((p, b, rows, d), generator=g).to(torch.bfloat16)
+    k = torch.randn((b, 1, n, d), generator=g).to(torch.bfloat16)
+    pk, _, table = I.to_paged(k, None, page, seed=9)
+    bad_seq, bad_page = 1, 3
+    table[bad_seq, bad_page] = pk.shape[0] + 5
+    s = H.score(q.to(DEV), [pk.to(DEV)], [0], 0.1, n, page_tables=[table.to(DEV)])
+    assert N.dustin_device_status() & 2
+    gone = np.arange(bad_page * page, min(n, (bad_page + 1) * page))
+    keep = np.setdiff1d(np.arange(n), gone)
+    for bb in range(b):
+        kb = H.f64(k[bb:bb + 1, 0])
+        cols = keep if bb == bad_seq else np.arange(n)
+        ref = np.zeros(n)
+        ref[cols] = O.score_heads([H.f64(q[0, bb:bb + 1])], [kb[:, cols]], 0.1)[0]
+        np.testing.assert_allclose(H.f64(s[bb]), ref, rtol=2e-4, atol=1e-7)
 
 
 def test_score_heads_unaligned_output():

@@ -140,3 +140,29 @@ def test_full_attention(step):
                                                H.f64(k[b:b + 1]),
                                                H.f64(v[b:b + 1]), wl.scale)
         H.assert_attn_close(o[b:b + 1], lse[b:b + 1], o_ref, l_ref)
+
+
+@pytest.mark.parametrize("k", [8192, 16384])
+def test_attention_at_the_longest_context(k):
+    """n = 65536 (the longest supported context), 72B head shape, k up to
+    a quarter of it: sparse and dense attention against the oracle."""
+    build.build()
+    N.load()
+    b, hq, hkv, d, w, n = 2, 64, 8, 128, 5, 65536
+    g = I.generator(k)
+    q = torch.randn((b, hq, w, d), generator=g).to(torch.bfloat16)
+    kk = torch.randn((b, hkv, n, d), generator=g).to(torch.bfloat16)
+    v = torch.randn((b, hkv, n, d), generator=g).to(torch.bfloat16)
+    idx = I.random_sorted_indices(b, n, k, seed=k + 1)
+    scale = d ** -0.5
+    o, lse = H.sparse_attn(q.to(DEV), kk.to(DEV), v.to(DEV), idx.to(DEV), scale)
+    o_f, l_f = H.full_attn(q.to(DEV), kk.to(DEV), v.to(DEV), scale)
+    assert N.dustin_device_status() == 0
+    for bb in range(b):
+        o_ref, l_ref = O.verify_attention(H.f64(q[bb:bb + 1]), H.f64(kk[bb:bb + 1]),
+                                          H.f64(v[bb:bb + 1]), idx[bb:bb + 1].numpy(),
+                                          scale)
+        H.assert_attn_close(o[bb:bb + 1], lse[bb:bb + 1], o_ref, l_ref)
+    o_ref, l_ref = O.full_verify_attention(H.f64(q[:1]), H.f64(kk[:1]), H.f64(v[:1]),
+                                           scale)
+    H.assert_attn_close(o_f[:1], l_f[:1], o_ref, l_ref)

@@ -320,12 +320,13 @@ struct ScoreTmaArgs {
 };
 
 // Build-time tunables: TMA pipeline depth per CTA (several CTAs share an
-// SM, each consuming its own tile).
+// SM, each consuming its own tile).  Measured at the 72B shape: d = 64 with
+// 3 stages 65.2 us per draft scoring call against 67.6 with 4, 69.3 with 6.
 #ifndef DUSTIN_SCORE_STAGES128
 #define DUSTIN_SCORE_STAGES128 3
 #endif
 #ifndef DUSTIN_SCORE_STAGES64
-#define DUSTIN_SCORE_STAGES64 4
+#define DUSTIN_SCORE_STAGES64 3
 #endif
 
 template <int D>

@@ -1,7 +1,7 @@
 // Sparse verification attention of many layers in one persistent launch
-// (the survey's NEXT-1: Stage 2 of the "dustin-long-context" notes, section
-// 2.2 / Fig. 5, for several layers whose queries are all ready; one global
-// index set serves every layer and head).
+// (Stage 2 of the "dustin-long-context" notes, section 2.2 / Fig. 5, for
+// several layers whose queries are all ready; one global index set serves
+// every layer and head).
 //
 // A work item is (layer, sequence b, kv head g, row block): the G*w query
 // rows of kv head g against the k selected positions of that layer's cache.

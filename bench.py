@@ -275,8 +275,9 @@ class Replica:
 
 def run_extras(rep, wl, dev, stream, L, args, t_attn, t_dense):
     """Per-layer times of the window-merge entry points (the w x w causal
-    block as one more tile of the same launch), and one step of the naive
-    estimator: every target query head of every layer scored."""
+    block as one more tile of the same launch), the multi-layer launch, one
+    step of the naive estimator (every target head of every layer and every
+    draft head of every draft layer scored) and of Quest-16."""
     import torch
     from sparse_kv_verification_gb300 import native as N
     inp = rep.inp
@@ -325,6 +326,21 @@ def run_extras(rep, wl, dev, stream, L, args, t_attn, t_dense):
     naive = [N.prepare_score_heads(q_all, [N.kv_desc(inp.k[l])] * hq, heads,
                                    wl.scale, s_out, ws, wl.n) for l in range(L)]
     t_naive_layer = time_pass(naive, 1)
+    # ... and the draft side: all draft query heads of each draft layer with
+    # their Gamma lookahead rows (distinct draft key buffers cycled).
+    nbuf_d = min(wl.draft_layers, 6)
+    k_draft = [torch.randn((wl.b, wl.draft_hkv, wl.n, wl.draft_d), generator=g,
+                           device=dev).to(torch.bfloat16) for _ in range(nbuf_d)]
+    q_dall = torch.randn((wl.draft_hq, wl.b, wl.gamma, wl.draft_d), generator=g,
+                         device=dev).to(torch.bfloat16)
+    ws_nd = N.workspace(N.dustin_score_heads_workspace_size(wl.b, wl.n, wl.draft_hq,
+                                                            wl.gamma), dev)
+    heads_d = [h // wl.draft_group for h in range(wl.draft_hq)]
+    naive_d = [N.prepare_score_heads(q_dall, [N.kv_desc(k_draft[l % nbuf_d])] * wl.draft_hq,
+                                     heads_d, wl.draft_scale, s_out, ws_nd, wl.n)
+               for l in range(wl.draft_layers)]
+    t_naive_draft_layer = time_pass(naive_d, 1)
+    del k_draft
     # Quest-16: page statistics (kept up to date at append time in Quest, so
     # timed apart) and, per step and layer, page scores for every query head
     # (latest-token query) plus the top k/16 pages per (sequence, head).
@@ -370,12 +386,16 @@ def run_extras(rep, wl, dev, stream, L, args, t_attn, t_dense):
             "stats_build_us_per_layer": t_stats,
         },
         "naive_estimator": {
-            "what": (f"all {hq} target query heads of each of {L} layers scored "
-                     "(latest-token query), one scoring call per layer; draft "
-                     "side not included"),
-            "ms_per_step": t_naive_layer * L / 1e3,
+            "what": (f"all {hq} target query heads of each of {L} layers (latest-"
+                     f"token query) and all {wl.draft_hq} draft heads of each of "
+                     f"{wl.draft_layers} draft layers ({wl.gamma} lookahead rows) "
+                     "scored, one scoring call per layer"),
+            "ms_per_step": (t_naive_layer * L + t_naive_draft_layer * wl.draft_layers) / 1e3,
+            "target_ms_per_step": t_naive_layer * L / 1e3,
+            "draft_ms_per_step": t_naive_draft_layer * wl.draft_layers / 1e3,
             "dense_attention_ms_per_step": (t_dense * L / 1e3) if t_dense else None,
-            "ratio_to_dense": (t_naive_layer / t_dense) if t_dense else None,
+            "ratio_to_dense": ((t_naive_layer * L + t_naive_draft_layer * wl.draft_layers)
+                               / (t_dense * L)) if t_dense else None,
         },
     }
 

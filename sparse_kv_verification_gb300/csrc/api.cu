@@ -481,6 +481,8 @@ int dustin_score_heads(int b, int n, int d, int n_pairs, int rows,
   for (int p = 0; p < n_pairs; ++p) {
     a.pairs[p].kv = to_view(kv[p]);
     a.pairs[p].kv_head = kv_head[p];
+    for (int q = 0; q < p; ++q)
+      if (kv[q].k == kv[p].k && kv_head[q] == kv_head[p]) a.keys_shared = 1;
   }
   cudaError_t e = launch_score(a, d, paged, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, what);

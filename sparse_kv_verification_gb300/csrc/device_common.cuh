@@ -169,6 +169,12 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(p));
   return p;
 }
+// L2 policy: the default eviction priority.
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;\n" : "=l"(p));
+  return p;
+}
 // Arrives on `bar` once every cp.async this thread issued so far has landed
 // (the barrier's expected count includes this arrival).
 __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {

@@ -26,6 +26,7 @@ struct ScoreArgs {
   int b, n, n_pairs, rows;
   int chunk, nchunks;
   float scale_log2;
+  int keys_shared;         // two pairs read the same keys (same cache, kv head)
   ScorePair pairs[kMaxPairs];
 };
 

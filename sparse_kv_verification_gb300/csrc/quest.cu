@@ -9,11 +9,13 @@
 //    owns D/32 channels and folds the page's rows into fp32 minima and
 //    maxima, written back as bf16 (exact: they are bf16 inputs).  Stats
 //    layout [b][h_kv][P][2][D] (minimum row, then maximum row).
-//  * quest_score_kernel: one thread per page of one (sequence, kv head),
-//    for all G query heads of that kv head; the G query rows sit in shared
-//    memory as fp32 and are read as broadcasts, the page's two stat rows
-//    stream through 16-byte loads.  max(q_c mn_c, q_c mx_c) is taken as
-//    q_c * (q_c >= 0 ? mx_c : mn_c), summed over channels in ascending order.
+//  * quest_score_kernel: one warp per 32 pages of one (sequence, kv head),
+//    for all G query heads of that kv head; each lane owns D/32 channels of
+//    a page's two stat rows (coalesced loads) and of the G query rows (fp32
+//    in shared memory), forms q_c * (q_c >= 0 ? mx_c : mn_c) summed over its
+//    channels, and the heads' sums over the lanes are taken eight at a time
+//    by a shuffle reduce-scatter; results leave as one store per head and
+//    32 pages.
 #include "device_common.cuh"
 #include "dustin.h"
 #include "internal.h"
@@ -95,57 +97,106 @@ __global__ void __launch_bounds__(256) quest_stats_kernel(const QuestArgs a) {
   }
 }
 
-constexpr int kScoreThreads = 128;
+constexpr int kScoreWarps = 8;
+constexpr int kPagesPerWarp = 32;
+constexpr int kPagesPerCta = kScoreWarps * kPagesPerWarp;
 constexpr int kHeadChunk = 8;
 
+// Sum over the 32 lanes of eight values per lane, leaving the sum of value
+// (lane >> 2) & 7 on every lane (nine shuffles: halves exchanged at lane
+// distances 16, 8, 4, then a plain sum over distances 2 and 1).
+__device__ __forceinline__ float reduce8(const float (&v)[kHeadChunk], int lane) {
+  float a[4], b[2];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const bool hi = lane & 16;
+    const float mine = hi ? v[i + 4] : v[i], other = hi ? v[i] : v[i + 4];
+    a[i] = mine + __shfl_xor_sync(0xffffffffu, other, 16);
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const bool hi = lane & 8;
+    const float mine = hi ? a[i + 2] : a[i], other = hi ? a[i] : a[i + 2];
+    b[i] = mine + __shfl_xor_sync(0xffffffffu, other, 8);
+  }
+  const bool hi = lane & 4;
+  float c = (hi ? b[1] : b[0]) + __shfl_xor_sync(0xffffffffu, hi ? b[0] : b[1], 4);
+  c += __shfl_xor_sync(0xffffffffu, c, 2);
+  c += __shfl_xor_sync(0xffffffffu, c, 1);
+  return c;
+}
+
+// One warp per 32 consecutive pages of one (sequence, kv head); lane l owns
+// channels [l D/32, (l + 1) D/32) of each page's two stat rows (coalesced
+// loads), forms its part of every head's bound, and the eight heads of a
+// chunk are summed over the lanes together (reduce8).  A page's bounds go
+// to shared memory and each head's 32 pages leave as one 128-byte store.
 template <int D>
-__global__ void __launch_bounds__(kScoreThreads)
+__global__ void __launch_bounds__(kScoreWarps * 32)
     quest_score_kernel(const QuestArgs a) {
-  extern __shared__ float sq[];   // [G][D] fp32 query rows of this kv head
-  const int tid = threadIdx.x;
-  const int blocks_per_head = (a.n_pages + kScoreThreads - 1) / kScoreThreads;
+  constexpr int CPL = D / 32;   // channels per lane
+  extern __shared__ float sq[];  // [G][D] fp32 query rows, then [warps][8][32]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int blocks_per_head = (a.n_pages + kPagesPerCta - 1) / kPagesPerCta;
   const int pb = blockIdx.x % blocks_per_head;
   const int g = (blockIdx.x / blocks_per_head) % a.hkv;
   const int bb = blockIdx.x / (blocks_per_head * a.hkv);
   const int group = a.hq / a.hkv;
+  float* res = sq + group * D + warp * kHeadChunk * 32;
   griddep_wait();
   griddep_launch_dependents();
-  for (int i = tid; i < group * D; i += kScoreThreads) {
+  for (int i = tid; i < group * D; i += kScoreWarps * 32) {
     const int h = g * group + i / D;
     sq[i] = __bfloat162float(a.q[((long long)bb * a.hq + h) * D + i % D]);
   }
   __syncthreads();
-  const int p = pb * kScoreThreads + tid;
-  if (p >= a.n_pages) return;
-  const __nv_bfloat16* st =
-      a.stats_in + (((long long)bb * a.hkv + g) * a.n_pages + p) * 2 * D;
+  const int p0 = pb * kPagesPerCta + warp * kPagesPerWarp;
+  if (p0 >= a.n_pages) return;
+  const int np = min(kPagesPerWarp, a.n_pages - p0);
+  const __nv_bfloat16* st0 =
+      a.stats_in + (((long long)bb * a.hkv + g) * a.n_pages + p0) * 2 * D + lane * CPL;
   for (int h0 = 0; h0 < group; h0 += kHeadChunk) {
     const int nh = min(kHeadChunk, group - h0);
-    float acc[kHeadChunk];
-#pragma unroll
-    for (int h = 0; h < kHeadChunk; ++h) acc[h] = 0.f;
-    for (int c0 = 0; c0 < D; c0 += 8) {
-      const uint4 umn = __ldg(reinterpret_cast<const uint4*>(st + c0));
-      const uint4 umx = __ldg(reinterpret_cast<const uint4*>(st + D + c0));
-      __nv_bfloat16 vmn[8], vmx[8];
-      memcpy(vmn, &umn, 16);
-      memcpy(vmx, &umx, 16);
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const float fmn = __bfloat162float(vmn[c]), fmx = __bfloat162float(vmx[c]);
-#pragma unroll
-        for (int h = 0; h < kHeadChunk; ++h) {
-          if (h < nh) {
-            const float qc = sq[(h0 + h) * D + c0 + c];
-            acc[h] = fmaf(qc, qc >= 0.f ? fmx : fmn, acc[h]);
-          }
-        }
-      }
-    }
+    float qv[kHeadChunk][CPL];
 #pragma unroll
     for (int h = 0; h < kHeadChunk; ++h)
-      if (h < nh)
-        a.scores[(((long long)bb * a.hq + g * group + h0 + h) * a.n_pages) + p] = acc[h];
+#pragma unroll
+      for (int c = 0; c < CPL; ++c)
+        qv[h][c] = h < nh ? sq[(h0 + h) * D + lane * CPL + c] : 0.f;
+    for (int pp = 0; pp < np; ++pp) {
+      const __nv_bfloat16* st = st0 + (long long)pp * 2 * D;
+      __nv_bfloat16 vmn[CPL], vmx[CPL];
+      if constexpr (CPL == 4) {
+        const uint2 umn = __ldg(reinterpret_cast<const uint2*>(st));
+        const uint2 umx = __ldg(reinterpret_cast<const uint2*>(st + D));
+        memcpy(vmn, &umn, 8);
+        memcpy(vmx, &umx, 8);
+      } else {
+        const uint32_t umn = __ldg(reinterpret_cast<const uint32_t*>(st));
+        const uint32_t umx = __ldg(reinterpret_cast<const uint32_t*>(st + D));
+        memcpy(vmn, &umn, 4);
+        memcpy(vmx, &umx, 4);
+      }
+      float part[kHeadChunk];
+#pragma unroll
+      for (int h = 0; h < kHeadChunk; ++h) {
+        float acc = 0.f;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+          const float qc = qv[h][c];
+          acc = fmaf(qc, __bfloat162float(qc >= 0.f ? vmx[c] : vmn[c]), acc);
+        }
+        part[h] = acc;
+      }
+      const float sum = reduce8(part, lane);
+      if ((lane & 3) == 0) res[((lane >> 2) & 7) * 32 + pp] = sum;
+    }
+    __syncwarp();
+    for (int h = 0; h < nh; ++h)
+      if (lane < np)
+        a.scores[((long long)bb * a.hq + g * group + h0 + h) * a.n_pages + p0 + lane] =
+            res[h * 32 + lane];
+    __syncwarp();
   }
 }
 
@@ -160,13 +211,13 @@ cudaError_t run_stats(const QuestArgs& a, cudaStream_t st) {
 
 template <int D>
 cudaError_t run_scores(const QuestArgs& a, cudaStream_t st) {
-  const int bph = (a.n_pages + kScoreThreads - 1) / kScoreThreads;
+  const int bph = (a.n_pages + kPagesPerCta - 1) / kPagesPerCta;
   const long long grid = (long long)a.b * a.hkv * bph;
-  const int smem = (a.hq / a.hkv) * D * 4;
+  const int smem = ((a.hq / a.hkv) * D + kScoreWarps * kHeadChunk * 32) * 4;
   cudaError_t e = cudaFuncSetAttribute(quest_score_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(quest_score_kernel<D>, dim3((unsigned)grid), dim3(kScoreThreads), smem,
+  e = launch_pdl(quest_score_kernel<D>, dim3((unsigned)grid), dim3(kScoreWarps * 32), smem,
                  st, a);
   if (e == cudaSuccess) note_launches(1);
   return e;

@@ -74,6 +74,8 @@ typedef enum dustin_status {
  * p = page_table[b*pages_per_seq + j/page_size] at
  * base + p*stride_b + h*stride_h + (j % page_size)*stride_n + c, so stride_b
  * is then the stride between pages.  page_table is a device int32 array.
+ * page_size is a positive multiple of 16 (scoring reads pages of 16, 32 or
+ * 64 positions as one TMA box each; other sizes take a cp.async path).
  * v may be NULL for calls that read keys only (scoring).
  * Strides are in elements; every stride must be a multiple of 8 (16 bytes).
  */

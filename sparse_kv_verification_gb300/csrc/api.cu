@@ -141,6 +141,26 @@ AttnPlan plan_units(int hq, int hkv, int w, int b, int npos) {
 // more positions than one CTA's row table holds (8192, or 4096 with four
 // row tiles), the positions of each unit are split into equal ranges and
 // merged by a combine kernel.
+// Row-table bytes of the sparse kernel's CTA for (d, row tiles), taken
+// from the kernel's configuration so that host planning and shared-memory
+// layout cannot drift apart.
+long long attn_tab_bytes(int d, int mt) {
+  if (d == 64) {
+    switch (mt) {
+      case 1: return AttnCfg<64, 1>::TAB_BYTES;
+      case 2: return AttnCfg<64, 2>::TAB_BYTES;
+      case 3: return AttnCfg<64, 3>::TAB_BYTES;
+      default: return AttnCfg<64, 4>::TAB_BYTES;
+    }
+  }
+  switch (mt) {
+    case 1: return AttnCfg<128, 1>::TAB_BYTES;
+    case 2: return AttnCfg<128, 2>::TAB_BYTES;
+    case 3: return AttnCfg<128, 3>::TAB_BYTES;
+    default: return AttnCfg<128, 4>::TAB_BYTES;
+  }
+}
+
 AttnPlan plan_sparse(int b, int hq, int hkv, int d, int w, int k, bool win) {
   AttnPlan p = plan_units(hq, hkv, w, b, k);
   const int tiles = (k + 63) / 64;
@@ -151,10 +171,10 @@ AttnPlan plan_sparse(int b, int hq, int hkv, int d, int w, int k, bool win) {
     const long long slots = (long long)attn_slots(false, d, p.mt);
     long long s = p.units >= slots ? 1 : slots / p.units;
     s = std::min<long long>(s, tiles);
-    // Row table of one CTA (the kernel's TAB_BYTES): 64-bit offsets for up
-    // to cap64 tiles, 32-bit row codes (the WIDE variant; not with the
+    // Row table of one CTA (the kernel's own TAB_BYTES): 64-bit offsets for
+    // up to cap64 tiles, 32-bit row codes (the WIDE variant; not with the
     // window) for up to cap32.
-    const long long tab_bytes = p.mt == 4 ? 16384 : 32768;
+    const long long tab_bytes = attn_tab_bytes(d, p.mt);
     const long long cap64 = tab_bytes / 8 / 64, cap32 = tab_bytes / 4 / 64;
     long long ct = (tiles + s - 1) / s;
     if (ct > cap64) {

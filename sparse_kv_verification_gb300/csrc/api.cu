@@ -215,7 +215,7 @@ AttnPlan plan_dense(int b, int hq, int hkv, int d, int w, int n, bool win) {
 #if DUSTIN_ATTN_GRID_CAP > 0
   slots = std::min<long long>(slots, DUSTIN_ATTN_GRID_CAP);
 #endif
-  const long long cap = 2048 / 4;
+  const long long cap = SkCfg<128, 3>::MAX_TILES;   // tiles one CTA's page table holds
   p.grid = std::max(std::min(slots, T), (T + cap - 1) / cap);
   // Every range boundary c T / G falls on a unit boundary when G divides
   // the unit count (conservatively "split" otherwise).
@@ -599,8 +599,9 @@ int dustin_sparse_verify_attn_layers(int n_layers, int b, int h_q, int h_kv, int
   if (rc) return rc;
   if (k < 0 || k > n)
     return fail(DUSTIN_ERR_SHAPE, "%s: k=%d must be in [0, n=%d]", what, k, n);
-  if (k > 2048)
-    return fail(DUSTIN_ERR_UNSUPPORTED, "%s: k=%d (at most 2048 per call)", what, k);
+  constexpr int kMlMaxK = SkCfg<128, 3>::MAX_TAB;   // offset-table entries of one item
+  if (k > kMlMaxK)
+    return fail(DUSTIN_ERR_UNSUPPORTED, "%s: k=%d (at most %d per call)", what, k, kMlMaxK);
   if (n_layers == 0 || b == 0) return DUSTIN_OK;
   if (!q || !kv || !o || !lse)
     return fail(DUSTIN_ERR_INVALID_ARG, "%s: q, kv, o and lse arrays are required", what);

@@ -757,14 +757,14 @@ def run_ours(args):
     if not args.no_e2e:
         inp = rep.inp
         L = rep.L
-        # Chunks of up to 6 layers, shrinking to 4, 2, 1, 1 layers at the
+        # Chunks of up to 8 layers, shrinking to 4, 2, 1, 1 layers at the
         # end, so that little output is left to copy after the last kernel.
         tail = []
         for size in (1, 1, 2, 4):
             if sum(tail) + size <= L // 2:
                 tail.insert(0, size)
         head = L - sum(tail)
-        n_head = -(-head // 6) if head else 0
+        n_head = -(-head // 8) if head else 0
         sizes = [head * (c + 1) // n_head - head * c // n_head
                  for c in range(n_head)] + tail
         bounds = [0]

@@ -500,6 +500,13 @@ SELECT_CASES = [
     # gets a smaller cluster
     (16, 32768, 2048, 4, 64, 0.5, -1, 1, True),
     (16, 20000, 3000, 2, 8, 0.7, 600, 1, True),
+    # many short rows (at least 304 of at most 4096 positions): the
+    # 256-thread CTAs, one per row
+    (400, 2048, 128, 0, 0, 1.0, -1, 0, True),
+    (320, 3000, 500, 4, 16, 0.5, -1, 1, True),
+    (310, 1000, 100, 2, 8, 0.5, 50, 1, False),
+    (304, 4096, 700, 4, 64, 0.3, -1, 1, True),
+    (303, 2048, 128, 0, 0, 1.0, -1, 0, True),
 ]
 
 

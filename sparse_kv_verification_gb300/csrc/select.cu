@@ -5,7 +5,8 @@
 //
 // One thread-block cluster of C <= 8 CTAs (1024 threads each) per sequence;
 // CTA r owns the positions [r seg, r seg + seg), seg a multiple of 32, so a
-// 32k-position row keeps 8 SMs busy instead of one.  Cluster-wide values
+// 32k-position row keeps 8 SMs busy instead of one.  Many short rows take
+// one 256-thread CTA each instead (the same code, fewer threads).  Cluster-wide values
 // pass through distributed shared memory: the CTAs publish partial results
 // in their own shared memory, barrier.cluster, then every CTA reads all the
 // partials in the same rank order, so every CTA derives the same values.

@@ -543,7 +543,6 @@ def run_sweep(args):
 def oracle_worker(args):
     """Runs inside a fresh single-threaded process: the CPU oracle on a
     bounded sample (a few sequences, a few layers) of the workload."""
-    import numpy as np
     import torch
     torch.set_num_threads(1)
     from oracle import dustin_oracle as O

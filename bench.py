@@ -614,6 +614,24 @@ def run_oracle_leg(args, reps, warmup):
 
 # ----------------------------------------------------------------- arms
 
+def e2e_chunk_bounds(L):
+    """Layer boundaries of the end-to-end copy chunks: chunks of up to 8
+    layers, shrinking to 4, 2, 1, 1 layers at the end, so that little output
+    is left to copy after the last kernel."""
+    tail = []
+    for size in (1, 1, 2, 4):
+        if sum(tail) + size <= L // 2:
+            tail.insert(0, size)
+    head = L - sum(tail)
+    n_head = -(-head // 8) if head else 0
+    sizes = [head * (c + 1) // n_head - head * c // n_head
+             for c in range(n_head)] + tail
+    bounds = [0]
+    for size in sizes:
+        bounds.append(bounds[-1] + size)
+    return bounds
+
+
 def l2_note(wl, n_layers):
     """How the timed steps avoid reading from a warm L2 (129 MB)."""
     layer_gb = wl.b * wl.hkv * wl.n * wl.d * 2 * 2 / 1e9
@@ -765,20 +783,8 @@ def run_ours(args):
     if not args.no_e2e:
         inp = rep.inp
         L = rep.L
-        # Chunks of up to 8 layers, shrinking to 4, 2, 1, 1 layers at the
-        # end, so that little output is left to copy after the last kernel.
-        tail = []
-        for size in (1, 1, 2, 4):
-            if sum(tail) + size <= L // 2:
-                tail.insert(0, size)
-        head = L - sum(tail)
-        n_head = -(-head // 8) if head else 0
-        sizes = [head * (c + 1) // n_head - head * c // n_head
-                 for c in range(n_head)] + tail
-        bounds = [0]
-        for size in sizes:
-            bounds.append(bounds[-1] + size)
-        n_chunks = len(sizes)
+        bounds = e2e_chunk_bounds(L)
+        n_chunks = len(bounds) - 1
         h_qt, h_qd = inp.q_t.cpu().pin_memory(), inp.q_d.cpu().pin_memory()
         h_q = rep.q_all.cpu().pin_memory()
         h_o = torch.empty(rep.o_all.shape, dtype=rep.o_all.dtype, pin_memory=True)

@@ -36,3 +36,16 @@ def test_reference_arm_line():
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
     # the tiny workload fits in L2 and says so
     assert "within L2" in d["config"]["l2"]
+
+
+def test_e2e_chunk_bounds():
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench", os.path.join(ROOT, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    assert bench.e2e_chunk_bounds(80) == [0, 8, 16, 24, 32, 40, 48, 56, 64, 72, 76, 78, 79, 80]
+    for L in range(1, 130):
+        b = bench.e2e_chunk_bounds(L)
+        sizes = [y - x for x, y in zip(b, b[1:])]
+        assert b[0] == 0 and b[-1] == L and all(s >= 1 for s in sizes)
+        assert max(sizes) <= 8 and sizes[-1] == 1

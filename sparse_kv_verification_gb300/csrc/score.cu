@@ -5,11 +5,14 @@
 //
 //   S[b][j] = sum_p sum_r softmax_j(scale * q[p][b][r] . K_p[b][g_p][j])
 //
-// Two passes.  Pass 1 (score_logits_kernel): one CTA per (pair, sequence,
-// 2048-position chunk) streams the chunk's key rows through a 4-stage
-// cp.async pipeline into swizzled shared memory, computes the rows' logits
-// with bf16 mma.sync (fp32 accumulate), writes them (log2 units) to the
-// workspace and keeps an online (max, sum of 2^(l - max)) per row.
+// Two passes.  Pass 1 computes each row's logits (log2 units) with bf16
+// mma.sync (fp32 accumulate), writes them to the workspace and keeps an
+// online (max, sum of 2^(l - max)) per row and 512-position chunk: the
+// persistent TMA kernel (score_logits_tma_kernel, below) for contiguous
+// caches and for pages of 16, 32 or 64 positions; otherwise
+// score_logits_kernel, one CTA per (pair, sequence, chunk) streaming the
+// chunk's key rows through a 4-stage cp.async pipeline into swizzled shared
+// memory.
 // Pass 2 (score_reduce_kernel): combines the chunk statistics into each
 // row's log2-sum-exp and writes S[b][j] = sum_{p,r} 2^(l - lse2), summed
 // in a fixed order (pair-major, then row) in fp32, four positions per

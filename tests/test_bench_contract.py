@@ -49,3 +49,19 @@ def test_e2e_chunk_bounds():
         sizes = [y - x for x, y in zip(b, b[1:])]
         assert b[0] == 0 and b[-1] == L and all(s >= 1 for s in sizes)
         assert max(sizes) <= 8 and sizes[-1] == 1
+
+
+def test_committed_sparse_profile_fields():
+    """The ncu summary the bench reads its traffic figure from names the
+    kernel source it was taken on and a per-launch DRAM traffic close to
+    the algorithmic bytes."""
+    text = open(os.path.join(ROOT, "profiles", "sparse_verify_attn_72b.md")).read()
+    vals = {}
+    for line in text.splitlines():
+        if line.strip().startswith("- ") and ":" in line:
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    assert len(vals["source_sha"]) == 16
+    traffic = float(vals["dram_bytes_per_launch_full"])
+    algorithmic = float(vals["algorithmic_bytes_per_launch"])
+    assert algorithmic <= traffic <= 1.1 * algorithmic

@@ -144,3 +144,32 @@ def test_score_and_select_validation(lib):
     assert sel(m=3, sd=None) == 1
     assert sel(n=(1 << 20) + 1) == 3
     assert sel(b=0) == 0 and sel(k=0) == 0
+
+
+def test_quest_and_window_validation(lib):
+    stats = ctypes.c_void_p(FAKE)
+    pst = lambda **kw: lib.dustin_quest_page_stats(
+        kw.get("b", 1), kw.get("hkv", 2), kw.get("d", 128), kw.get("n", 256),
+        kw.get("page", 16), ctypes.byref(kw.get("kv", kv())), kw.get("st", FAKE), None)
+    assert pst(d=96) == 3
+    assert pst(page=0) == 2
+    assert pst(st=FAKE + 4) == 5
+    assert pst(b=0) == 0
+    psc = lambda **kw: lib.dustin_quest_page_scores(
+        kw.get("b", 1), kw.get("hq", 8), kw.get("hkv", 2), kw.get("d", 128),
+        kw.get("n", 256), kw.get("page", 16), kw.get("q", FAKE), kw.get("st", FAKE),
+        kw.get("sc", FAKE), None)
+    assert psc(hq=130, hkv=2) == 3          # more than 64 query heads per kv head
+    assert psc(hq=7) == 2                    # not a multiple of h_kv
+    assert psc(q=None) == 1
+    assert psc(st=FAKE + 8) == 5
+    assert psc(d=80) == 3
+    assert lib.dustin_quest_stats_size(2, 4, 128, 1000, 16) == 2 * 4 * 63 * 2 * 128 * 2
+    win = kv(stride_n=128)
+    wcall = lambda **kw: lib.dustin_sparse_verify_attn_window(
+        1, 8, 2, 128, 4, 256, 32, FAKE, ctypes.byref(kv()), FAKE,
+        ctypes.byref(kw.get("win", win)) if kw.get("win", win) is not None else None,
+        0.1, FAKE, FAKE, None, 0, kw.get("flags", 0), None)
+    assert wcall(win=None) == 1
+    assert wcall(win=kv(stride_n=100)) == 2
+    assert wcall(flags=4) == 1

@@ -147,7 +147,6 @@ def test_score_and_select_validation(lib):
 
 
 def test_quest_and_window_validation(lib):
-    stats = ctypes.c_void_p(FAKE)
     pst = lambda **kw: lib.dustin_quest_page_stats(
         kw.get("b", 1), kw.get("hkv", 2), kw.get("d", 128), kw.get("n", 256),
         kw.get("page", 16), ctypes.byref(kw.get("kv", kv())), kw.get("st", FAKE), None)

@@ -71,17 +71,13 @@ struct AttnArgs {
   float2* ws_ml;    // [blocks][splits][16 MT]    (m in log2 units, l)
 };
 
-// Build-time tunables (nvcc -D): producer warps (4 or 8), pipeline depth
-// for d = 128, and split accumulators for S = Q K^T (two half-depth chains
-// per n8 tile instead of one, for instruction-level parallelism).
+// Build-time tunables (nvcc -D): producer warps (4 or 8) and pipeline depth
+// for d = 128.
 #ifndef DUSTIN_ATTN_NPW
 #define DUSTIN_ATTN_NPW 4
 #endif
 #ifndef DUSTIN_ATTN_STAGES128
 #define DUSTIN_ATTN_STAGES128 5
-#endif
-#ifndef DUSTIN_ATTN_SPLIT_QK
-#define DUSTIN_ATTN_SPLIT_QK 0
 #endif
 #ifndef DUSTIN_ATTN_ROTATE
 #define DUSTIN_ATTN_ROTATE 1
@@ -437,13 +433,6 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
     for (int j = 0; j < C::NT8; ++j)
 #pragma unroll
       for (int e = 0; e < 4; ++e) sc[j][e] = 0.f;
-#if DUSTIN_ATTN_SPLIT_QK
-    float sc2[C::NT8][4];
-#pragma unroll
-    for (int j = 0; j < C::NT8; ++j)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) sc2[j][e] = 0.f;
-#endif
 #pragma unroll
     for (int ks = 0; ks < C::KS; ++ks) {
 #pragma unroll
@@ -452,23 +441,10 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
         const int ch = ks * 2 + ((lane >> 3) & 1);
         uint32_t b0, b1, b2, b3;
         ldmatrix_x4(smem_u32(tk + r * C::RS + ch * 16), b0, b1, b2, b3);
-#if DUSTIN_ATTN_SPLIT_QK
-        if (ks & 1) {
-          mma_bf16(sc2[j], qf[ks], b0, b1);
-          mma_bf16(sc2[j + 1], qf[ks], b2, b3);
-          continue;
-        }
-#endif
         mma_bf16(sc[j], qf[ks], b0, b1);
         mma_bf16(sc[j + 1], qf[ks], b2, b3);
       }
     }
-#if DUSTIN_ATTN_SPLIT_QK
-#pragma unroll
-    for (int j = 0; j < C::NT8; ++j)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) sc[j][e] += sc2[j][e];
-#endif
 
     // Rows left out of the tile get -inf.  Scores stay unscaled here: the
     // scale (> 0) is folded into the exponent below, so the maximum is taken

@@ -12,20 +12,9 @@ cudaError_t prepare() {
   using C = SkCfg<D, MT>;
   static std::atomic<uint64_t> done{0};
   if constexpr (C::REBALANCE) {
-    // setmaxnreg only redistributes the registers the block was launched
-    // with: refuse to launch if the compiled allocation could not cover the
-    // requested split (the increase would otherwise never complete).
     static std::atomic<int> checked{0};
-    if (checked.load() == 0) {
-      cudaFuncAttributes fa;
-      cudaError_t e = cudaFuncGetAttributes(&fa, verify_attn_sk_kernel<D, MT, PAGED, WIN>);
-      if (e != cudaSuccess) return e;
-      const long long have = (long long)fa.numRegs * C::NT;
-      const long long need = (long long)C::PRODUCER_REGS * C::NPW * 32 +
-                             (long long)C::CONSUMER_REGS * C::NCW * 32;
-      checked.store(have >= need ? 1 : -1);
-    }
-    if (checked.load() < 0) return cudaErrorInvalidConfiguration;
+    cudaError_t e = check_register_split<C>(verify_attn_sk_kernel<D, MT, PAGED, WIN>, checked);
+    if (e != cudaSuccess) return e;
   }
   return ensure_smem_attr(verify_attn_sk_kernel<D, MT, PAGED, WIN>, C::SMEM, done);
 }

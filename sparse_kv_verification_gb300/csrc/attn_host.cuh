@@ -15,20 +15,9 @@ struct AttnHost {
     using C = AttnCfg<D, MT>;
     static std::atomic<uint64_t> done{0};
     if constexpr (C::REBALANCE) {
-      // setmaxnreg only redistributes the registers the block was launched
-      // with: refuse to launch if the compiled allocation could not cover
-      // the requested split (the increase would otherwise never complete).
       static std::atomic<int> checked{0};
-      if (checked.load() == 0) {
-        cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, verify_attn_kernel<D, MT, PAGED, WIN, WIDE>);
-        if (e != cudaSuccess) return e;
-        const long long have = (long long)fa.numRegs * C::NT;
-        const long long need = (long long)C::PRODUCER_REGS * C::NPW * 32 +
-                               (long long)C::CONSUMER_REGS * C::NCW * 32;
-        checked.store(have >= need ? 1 : -1);
-      }
-      if (checked.load() < 0) return cudaErrorInvalidConfiguration;
+      cudaError_t e = check_register_split<C>(verify_attn_kernel<D, MT, PAGED, WIN, WIDE>, checked);
+      if (e != cudaSuccess) return e;
     }
     return ensure_smem_attr(verify_attn_kernel<D, MT, PAGED, WIN, WIDE>, C::SMEM, done);
   }

@@ -232,6 +232,28 @@ cudaError_t ensure_smem_attr(K kern, int bytes, std::atomic<uint64_t>& done) {
   return e;
 }
 
+// setmaxnreg only redistributes the registers a block was launched with.
+// Returns cudaErrorInvalidConfiguration, checked once per kernel instance
+// (`checked` caches the answer), when the compiled allocation of `kern`
+// cannot cover the producer/consumer register split of its configuration C
+// (NT threads; NPW producer warps at PRODUCER_REGS, NCW consumer warps at
+// CONSUMER_REGS): the consumers' increase would otherwise never complete.
+template <typename C, typename K>
+cudaError_t check_register_split(K kern, std::atomic<int>& checked) {
+  int v = checked.load();
+  if (v == 0) {
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    const long long have = (long long)fa.numRegs * C::NT;
+    const long long need = (long long)C::PRODUCER_REGS * C::NPW * 32 +
+                           (long long)C::CONSUMER_REGS * C::NCW * 32;
+    v = have >= need ? 1 : -1;
+    checked.store(v);
+  }
+  return v > 0 ? cudaSuccess : cudaErrorInvalidConfiguration;
+}
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block,
                        size_t smem, cudaStream_t st, Args&&... args) {

@@ -152,9 +152,14 @@ int dustin_score_heads(int b, int n, int d, int n_pairs, int rows,
  * allocates nothing.
  *   - A call whose scratch (dustin_score_heads_workspace_size) exceeds the
  *     array is rejected with DUSTIN_ERR_WORKSPACE before anything runs.
+ *   - The argument checks of dustin_score_heads run first (same statuses);
+ *     then a call whose scratch (dustin_score_heads_workspace_size) exceeds
+ *     the array is rejected with DUSTIN_ERR_WORKSPACE before anything runs.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     before any stream capture.  The address is remembered per device and
+ *     CUDA context: after cudaDeviceReset the next call looks it up again
+ *     (again outside any capture).
  *   - All calls share the one array, which keeps the last call's contents.
  *     Each call overwrites every scratch byte it reads, so nothing needs
  *     clearing, but calls that overlap on the GPU (other streams, other
@@ -165,6 +170,9 @@ int dustin_score_heads_noalloc(int b, int n, int d, int n_pairs, int rows,
                                const void* q, const dustin_kv* kv,
                                const int32_t* kv_head, float scale,
                                float* s_out, void* stream);
+/* Size in bytes of that built-in array (DUSTIN_NOALLOC_SCRATCH_BYTES of the
+ * library as built), for callers that plan around it at run time. */
+size_t dustin_score_heads_noalloc_capacity(void);
 
 /* ------------------------------------------------------------------------
  * Hybrid combination and global per-sequence Top-K ([Notes] sections 2.2

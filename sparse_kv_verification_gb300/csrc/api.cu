@@ -389,6 +389,48 @@ int run_attn(bool dense, int b, int hq, int hkv, int d, int w, int n, int k,
 
 }  // namespace
 
+// Argument checks of the scoring calls (everything but the workspace):
+// DUSTIN_OK with *empty set when there is nothing to do.
+int check_score_args(int b, int n, int d, int n_pairs, int rows, const void* q,
+                     const dustin_kv* kv, const int32_t* kv_head, float scale,
+                     const float* s_out, const char* what, bool* paged, bool* empty) {
+  *paged = false;
+  *empty = false;
+  if (b < 0 || n < 0) return fail(DUSTIN_ERR_SHAPE, "%s: b=%d n=%d", what, b, n);
+  if (d != 64 && d != 128)
+    return fail(DUSTIN_ERR_UNSUPPORTED, "%s: d=%d (64 or 128)", what, d);
+  if (n_pairs < 1 || n_pairs > kMaxPairs)
+    return fail(DUSTIN_ERR_UNSUPPORTED, "%s: n_pairs=%d (1..%d)", what, n_pairs,
+                kMaxPairs);
+  if (rows < 1 || rows > 16)
+    return fail(DUSTIN_ERR_UNSUPPORTED, "%s: rows=%d (1..16)", what, rows);
+  if (n_pairs * rows > 1024)
+    return fail(DUSTIN_ERR_UNSUPPORTED, "%s: n_pairs*rows > 1024", what);
+  if (b == 0 || n == 0) {
+    *empty = true;
+    return DUSTIN_OK;
+  }
+  if (!q || !kv || !kv_head || !s_out)
+    return fail(DUSTIN_ERR_INVALID_ARG, "%s: q, kv, kv_head, s_out required", what);
+  if (!aligned16(q) || (reinterpret_cast<uintptr_t>(s_out) & 3u))
+    return fail(DUSTIN_ERR_ALIGNMENT, "%s: q needs 16-byte alignment", what);
+  if (!std::isfinite(scale))
+    return fail(DUSTIN_ERR_INVALID_ARG, "%s: scale is not finite", what);
+  if ((long long)n_pairs * b * ((n + score_chunk() - 1) / score_chunk()) > 0x7fffffffLL ||
+      (long long)b > 65535)
+    return fail(DUSTIN_ERR_SHAPE, "%s: problem too large", what);
+  for (int p = 0; p < n_pairs; ++p) {
+    int rc = check_kv(&kv[p], b, n, d, false, what);
+    if (rc) return rc;
+    if (kv_head[p] < 0)
+      return fail(DUSTIN_ERR_SHAPE, "%s: kv_head[%d]=%d", what, p, kv_head[p]);
+    if (p > 0 && ((kv[p].page_table != nullptr) != *paged))
+      return fail(DUSTIN_ERR_UNSUPPORTED, "%s: mixed paged/contiguous pairs", what);
+    *paged = kv[p].page_table != nullptr;
+  }
+  return DUSTIN_OK;
+}
+
 void note_launches(int count) { g_launches.fetch_add((uint64_t)count); }
 
 int record_error(int status, const char* message) {
@@ -449,36 +491,10 @@ int dustin_score_heads(int b, int n, int d, int n_pairs, int rows,
                        const int32_t* kv_head, float scale, float* s_out,
                        void* ws, size_t ws_bytes, void* stream) {
   const char* what = "dustin_score_heads";
-  if (b < 0 || n < 0) return fail(DUSTIN_ERR_SHAPE, "%s: b=%d n=%d", what, b, n);
-  if (d != 64 && d != 128)
-    return fail(DUSTIN_ERR_UNSUPPORTED, "%s: d=%d (64 or 128)", what, d);
-  if (n_pairs < 1 || n_pairs > kMaxPairs)
-    return fail(DUSTIN_ERR_UNSUPPORTED, "%s: n_pairs=%d (1..%d)", what, n_pairs,
-                kMaxPairs);
-  if (rows < 1 || rows > 16)
-    return fail(DUSTIN_ERR_UNSUPPORTED, "%s: rows=%d (1..16)", what, rows);
-  if (n_pairs * rows > 1024)
-    return fail(DUSTIN_ERR_UNSUPPORTED, "%s: n_pairs*rows > 1024", what);
-  if (b == 0 || n == 0) return DUSTIN_OK;
-  if (!q || !kv || !kv_head || !s_out)
-    return fail(DUSTIN_ERR_INVALID_ARG, "%s: q, kv, kv_head, s_out required", what);
-  if (!aligned16(q) || (reinterpret_cast<uintptr_t>(s_out) & 3u))
-    return fail(DUSTIN_ERR_ALIGNMENT, "%s: q needs 16-byte alignment", what);
-  if (!std::isfinite(scale))
-    return fail(DUSTIN_ERR_INVALID_ARG, "%s: scale is not finite", what);
-  if ((long long)n_pairs * b * ((n + score_chunk() - 1) / score_chunk()) > 0x7fffffffLL ||
-      (long long)b > 65535)
-    return fail(DUSTIN_ERR_SHAPE, "%s: problem too large", what);
-  bool paged = false;
-  for (int p = 0; p < n_pairs; ++p) {
-    int rc = check_kv(&kv[p], b, n, d, false, what);
-    if (rc) return rc;
-    if (kv_head[p] < 0)
-      return fail(DUSTIN_ERR_SHAPE, "%s: kv_head[%d]=%d", what, p, kv_head[p]);
-    if (p > 0 && ((kv[p].page_table != nullptr) != paged))
-      return fail(DUSTIN_ERR_UNSUPPORTED, "%s: mixed paged/contiguous pairs", what);
-    paged = kv[p].page_table != nullptr;
-  }
+  bool paged = false, empty = false;
+  const int rc = check_score_args(b, n, d, n_pairs, rows, q, kv, kv_head, scale, s_out,
+                                  what, &paged, &empty);
+  if (rc || empty) return rc;
   const size_t need = dustin_score_heads_workspace_size(b, n, n_pairs, rows);
   if (!ws || ws_bytes < need || !aligned16(ws))
     return fail(DUSTIN_ERR_WORKSPACE, "%s: workspace %zu bytes, need %zu", what,

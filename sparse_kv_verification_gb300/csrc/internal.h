@@ -8,6 +8,8 @@
 
 #include "device_common.cuh"
 
+struct dustin_kv;
+
 namespace dustin {
 
 // ---- scoring
@@ -31,6 +33,9 @@ struct ScoreArgs {
 };
 
 int score_chunk();
+int check_score_args(int b, int n, int d, int n_pairs, int rows, const void* q,
+                     const ::dustin_kv* kv, const int32_t* kv_head, float scale,
+                     const float* s_out, const char* what, bool* paged, bool* empty);
 cudaError_t launch_score(const ScoreArgs& a, int d, bool paged, cudaStream_t st);
 cudaError_t take_score_flags(unsigned* flags);
 

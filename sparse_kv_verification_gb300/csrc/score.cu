@@ -753,33 +753,74 @@ namespace {
 static __device__ __align__(256) unsigned char
     g_noalloc_scratch[DUSTIN_NOALLOC_SCRATCH_BYTES];
 
-std::atomic<void*> g_noalloc_ptr[64];
+// The current context's id through the runtime's driver entry points (no
+// link against the driver library); 0 when there is no current context or
+// the entry points are missing.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+unsigned long long current_context_id() {
+  static std::atomic<void*> get_current{nullptr}, get_id{nullptr};
+  static std::atomic<int> tried{0};
+  if (!tried.load(std::memory_order_acquire)) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current.store(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id.store(p);
+    tried.store(1, std::memory_order_release);
+  }
+  auto cur = reinterpret_cast<CtxGetCurrentFn>(get_current.load());
+  auto id = reinterpret_cast<CtxGetIdFn>(get_id.load());
+  CUcontext ctx = nullptr;
+  unsigned long long v = 0;
+  if (!cur || !id || cur(&ctx) != CUDA_SUCCESS || !ctx || id(ctx, &v) != CUDA_SUCCESS) return 0;
+  return v;
+}
+
+// Device address of the array, per device, remembered together with the
+// context it was looked up in: a new context on that device (after
+// cudaDeviceReset, say) looks the address up again.  In host code the
+// array's name is only a host-side stand-in, so the kernels always get this
+// address.
+struct NoallocSlot {
+  void* ptr = nullptr;
+  unsigned long long ctx = 0;
+};
+NoallocSlot g_noalloc_slot[64];
 std::mutex g_noalloc_mutex;
 
-// Device address of the array on the current device, looked up once per
-// device (with that device current).  In host code the array's name is only
-// a host-side stand-in, so the kernels always get this address.
 cudaError_t noalloc_scratch(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  void* p = g_noalloc_ptr[dev].load(std::memory_order_acquire);
-  if (p == nullptr) {
-    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    p = g_noalloc_ptr[dev].load(std::memory_order_acquire);
-    if (p == nullptr) {
-      e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-      if (e != cudaSuccess) return e;
-      g_noalloc_ptr[dev].store(p, std::memory_order_release);
-    }
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  NoallocSlot& slot = g_noalloc_slot[dev];
+  const unsigned long long ctx = current_context_id();
+  if (slot.ptr == nullptr || ctx == 0 || ctx != slot.ctx) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    slot.ptr = p;
+    slot.ctx = current_context_id();   // the lookup made the context current
   }
-  *out = p;
+  *out = slot.ptr;
   return cudaSuccess;
 }
 
 }  // namespace
 }  // namespace dustin
+
+extern "C" size_t dustin_score_heads_noalloc_capacity(void) {
+  return (size_t)DUSTIN_NOALLOC_SCRATCH_BYTES;
+}
 
 extern "C" int dustin_score_heads_noalloc(int b, int n, int d, int n_pairs,
                                           int rows, const void* q,
@@ -787,26 +828,25 @@ extern "C" int dustin_score_heads_noalloc(int b, int n, int d, int n_pairs,
                                           const int32_t* kv_head, float scale,
                                           float* s_out, void* stream) {
   using namespace dustin;
+  const char* what = "dustin_score_heads_noalloc";
+  bool paged = false, empty = false;
+  const int rc = check_score_args(b, n, d, n_pairs, rows, q, kv, kv_head, scale, s_out,
+                                  what, &paged, &empty);
+  if (rc || empty) return rc;
   const size_t need = dustin_score_heads_workspace_size(b, n, n_pairs, rows);
   if (need > (size_t)DUSTIN_NOALLOC_SCRATCH_BYTES) {
     char msg[256];
     snprintf(msg, sizeof(msg),
-             "dustin_score_heads_noalloc: this call needs %zu bytes of scratch; "
-             "the built-in array holds %zu (use dustin_score_heads with a "
-             "workspace)",
-             need, (size_t)DUSTIN_NOALLOC_SCRATCH_BYTES);
+             "%s: this call needs %zu bytes of scratch; the built-in array holds %zu "
+             "(use dustin_score_heads with a workspace)",
+             what, need, (size_t)DUSTIN_NOALLOC_SCRATCH_BYTES);
     return record_error(DUSTIN_ERR_WORKSPACE, msg);
   }
-  if (need == 0)  // empty or invalid sizes: the checks of the main entry point
-    return dustin_score_heads(b, n, d, n_pairs, rows, q, kv, kv_head, scale,
-                              s_out, nullptr, 0, stream);
   void* ws = nullptr;
   cudaError_t e = noalloc_scratch(&ws);
   if (e != cudaSuccess) {
     char msg[256];
-    snprintf(msg, sizeof(msg),
-             "dustin_score_heads_noalloc: cudaGetSymbolAddress: %s",
-             cudaGetErrorString(e));
+    snprintf(msg, sizeof(msg), "%s: cudaGetSymbolAddress: %s", what, cudaGetErrorString(e));
     return record_error(DUSTIN_ERR_CUDA, msg);
   }
   return dustin_score_heads(b, n, d, n_pairs, rows, q, kv, kv_head, scale,

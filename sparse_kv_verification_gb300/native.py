@@ -24,7 +24,7 @@ EXPORTS = (
     "dustin_status_string", "dustin_last_error", "dustin_version",
     "dustin_launch_count", "dustin_device_status",
     "dustin_score_heads_workspace_size", "dustin_score_heads",
-    "dustin_score_heads_noalloc",
+    "dustin_score_heads_noalloc", "dustin_score_heads_noalloc_capacity",
     "dustin_hybrid_topk",
     "dustin_sparse_verify_attn_workspace_size", "dustin_sparse_verify_attn",
     "dustin_sparse_verify_attn_window",
@@ -90,6 +90,7 @@ def load(build_if_missing: bool = False, path: Optional[str] = None
         "dustin_score_heads_workspace_size": (S, [I, I, I, I]),
         "dustin_score_heads": (I, [I, I, I, I, I, P, P, P, F, P, P, S, P]),
         "dustin_score_heads_noalloc": (I, [I, I, I, I, I, P, P, P, F, P, P]),
+        "dustin_score_heads_noalloc_capacity": (S, []),
         "dustin_hybrid_topk": (I, [I, I, I, I, I, D, I, I, P, P, P, P]),
         "dustin_sparse_verify_attn_workspace_size": (S, [I, I, I, I, I, I]),
         "dustin_sparse_verify_attn": (I, [I, I, I, I, I, I, I, P, P, P, F, P, P,
@@ -190,13 +191,16 @@ def dustin_score_heads(q: torch.Tensor, kvs: Sequence[DustinKV],
         raise ValueError("q must be contiguous; s_out fp32")
     arr = (DustinKV * n_pairs)(*kvs)
     heads = (ctypes.c_int32 * n_pairs)(*[int(h) for h in kv_heads])
-    _check(load().dustin_score_heads(
-        b, n, d, n_pairs, rows, q.data_ptr(), ctypes.addressof(arr),
-        ctypes.addressof(heads), float(scale), s_out.data_ptr(), ws.data_ptr(),
-        ws.numel(), _stream(stream, q.device)))
+    with torch.cuda.device(q.device):
+        _check(load().dustin_score_heads(
+            b, n, d, n_pairs, rows, q.data_ptr(), ctypes.addressof(arr),
+            ctypes.addressof(heads), float(scale), s_out.data_ptr(), ws.data_ptr(),
+            ws.numel(), _stream(stream, q.device)))
 
 
-NOALLOC_SCRATCH_BYTES = 64 << 20
+def noalloc_scratch_bytes() -> int:
+    """Size of the library's built-in scoring scratch array."""
+    return int(load().dustin_score_heads_noalloc_capacity())
 
 
 def dustin_score_heads_noalloc(q: torch.Tensor, kvs: Sequence[DustinKV],
@@ -214,10 +218,12 @@ def dustin_score_heads_noalloc(q: torch.Tensor, kvs: Sequence[DustinKV],
         raise ValueError("q must be contiguous; s_out fp32")
     arr = (DustinKV * n_pairs)(*kvs)
     heads = (ctypes.c_int32 * n_pairs)(*[int(h) for h in kv_heads])
-    _check(load().dustin_score_heads_noalloc(
-        b, n, d, n_pairs, rows, q.data_ptr(), ctypes.addressof(arr),
-        ctypes.addressof(heads), float(scale), s_out.data_ptr(),
-        _stream(stream, q.device)))
+    # The library finds the array of the current device: make it q's.
+    with torch.cuda.device(q.device):
+        _check(load().dustin_score_heads_noalloc(
+            b, n, d, n_pairs, rows, q.data_ptr(), ctypes.addressof(arr),
+            ctypes.addressof(heads), float(scale), s_out.data_ptr(),
+            _stream(stream, q.device)))
 
 
 # ------------------------------------------------------------------ selection

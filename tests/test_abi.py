@@ -146,6 +146,27 @@ def test_score_and_select_validation(lib):
     assert sel(b=0) == 0 and sel(k=0) == 0
 
 
+def test_noalloc_checks_arguments_before_the_array_size(lib):
+    """The no-allocation scoring call gives the statuses of dustin_score_heads
+    for bad arguments even when their scratch would also overflow the
+    built-in array, and WORKSPACE only for valid calls that need more."""
+    assert lib.dustin_score_heads_noalloc_capacity() == native.noalloc_scratch_bytes()
+    cap = lib.dustin_score_heads_noalloc_capacity()
+    heads = (ctypes.c_int32 * 64)(*([0] * 64))
+    arr = (native.DustinKV * 64)(*([kv(stride_n=128)] * 64))
+    call = lambda b=16, n=32768, d=128, p=64, rows=1: lib.dustin_score_heads_noalloc(
+        b, n, d, p, rows, FAKE, ctypes.addressof(arr), ctypes.addressof(heads), 0.1,
+        FAKE, None)
+    assert lib.dustin_score_heads_workspace_size(16, 32768, 64, 1) > cap
+    assert call(d=96) == 3
+    assert call(rows=17) == 3
+    assert call(p=65) == 3
+    assert call(b=-1) == 2
+    assert call() == 4
+    assert str(cap) in lib.dustin_last_error().decode()
+    assert call(b=0) == 0
+
+
 def test_quest_and_window_validation(lib):
     pst = lambda **kw: lib.dustin_quest_page_stats(
         kw.get("b", 1), kw.get("hkv", 2), kw.get("d", 128), kw.get("n", 256),

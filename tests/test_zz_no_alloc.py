@@ -12,6 +12,7 @@ import numpy as np
 import pytest
 import torch
 
+from oracle import dustin_oracle as O
 from sparse_kv_verification_gb300 import build, inputs as I, native as N
 from tests import gpu_harness as H
 
@@ -49,18 +50,30 @@ def test_noalloc_matches_workspace_call_twice():
                                    atol=1e-7)
         np.testing.assert_allclose(H.f64(got).sum(axis=1), p * rows,
                                    rtol=1e-4)
+        # and against the oracle directly, at the scoring parity tolerance
+        want = O.score_heads([H.f64(q[i].cpu()) for i in range(p)],
+                             [H.f64(keys[i][:, heads[i]].cpu()) for i in range(p)],
+                             scale)
+        np.testing.assert_allclose(H.f64(got), want, rtol=2e-4, atol=1e-7)
 
 
 def test_noalloc_rejects_sizes_beyond_the_array():
+    """A valid call whose scratch would overflow the built-in array is
+    refused with DUSTIN_ERR_WORKSPACE before anything runs (the pointers
+    below are never dereferenced)."""
     lib = N.load()
-    heads = (ctypes.c_int32 * 64)(*([0] * 64))
-    arr = (N.DustinKV * 64)()
-    b, n, pairs, rows = 16, 65536, 64, 1          # 256 MiB of logits
+    b, n, pairs, rows, d = 16, 65536, 64, 1, 128  # 256 MiB of logits
+    heads = (ctypes.c_int32 * pairs)(*([0] * pairs))
+    desc = N.DustinKV()
+    desc.k = desc.v = 0x10000
+    desc.stride_n, desc.stride_h, desc.stride_b = d, n * d, 8 * n * d
+    arr = (N.DustinKV * pairs)(*([desc] * pairs))
     need = N.dustin_score_heads_workspace_size(b, n, pairs, rows)
-    assert need > N.NOALLOC_SCRATCH_BYTES
+    cap = N.noalloc_scratch_bytes()
+    assert need > cap
     status = lib.dustin_score_heads_noalloc(
-        b, n, 128, pairs, rows, 0x10000, ctypes.addressof(arr),
+        b, n, d, pairs, rows, 0x10000, ctypes.addressof(arr),
         ctypes.addressof(heads), 0.1, 0x10000, None)
     assert status == 4                            # DUSTIN_ERR_WORKSPACE
     msg = lib.dustin_last_error().decode()
-    assert str(N.NOALLOC_SCRATCH_BYTES) in msg and str(need) in msg
+    assert str(cap) in msg and str(need) in msg

@@ -52,16 +52,12 @@ def test_e2e_chunk_bounds():
 
 
 def test_committed_sparse_profile_fields():
-    """The ncu summary the bench reads its traffic figure from names the
+    """The ncu record the bench reads its traffic figure from names the
     kernel source it was taken on and a per-launch DRAM traffic close to
     the algorithmic bytes."""
-    text = open(os.path.join(ROOT, "profiles", "sparse_verify_attn_72b.md")).read()
-    vals = {}
-    for line in text.splitlines():
-        if line.strip().startswith("- ") and ":" in line:
-            k, v = line.strip()[2:].split(":", 1)
-            vals[k.strip()] = v.strip().strip("`")
-    assert len(vals["source_sha"]) == 16
-    traffic = float(vals["dram_bytes_per_launch_full"])
-    algorithmic = float(vals["algorithmic_bytes_per_launch"])
+    with open(os.path.join(ROOT, "profiles", "sparse_verify_attn_72b.json")) as f:
+        rec = json.load(f)
+    assert len(rec["source_sha"]) == 16
+    traffic = float(rec["dram_bytes_per_launch"])
+    algorithmic = float(rec["algorithmic_bytes_per_launch"])
     assert algorithmic <= traffic <= 1.1 * algorithmic

@@ -416,6 +416,31 @@ def test_score_heads_parity(p, b, rows, d, n):
     np.testing.assert_allclose(H.f64(s).sum(axis=1), p * rows, rtol=1e-4)
 
 
+@pytest.mark.parametrize("pairs,hkv,rows,d,n,b", [(64, 8, 1, 128, 8192, 2),
+                                                  (14, 2, 4, 64, 8192, 3)],
+                         ids=["target-all-heads", "draft-all-heads"])
+def test_score_heads_naive_estimator_shapes(pairs, hkv, rows, d, n, b):
+    """The naive estimator ([Paper] section 1, [Notes] section 3 Fig. 8)
+    scores every query head of a layer: 64 target heads with the latest
+    token's row, or the draft's 14 heads with its lookahead rows.  The
+    pairs then share their kv heads' keys (pairs // hkv siblings each),
+    which selects the kernel's shared-keys L2 policy; every element against
+    the oracle at the scoring tolerance."""
+    g = I.generator(pairs * 1000 + n)
+    keys = (2.0 * torch.randn((b, hkv, n, d), generator=g)).to(torch.bfloat16)
+    q = torch.randn((pairs, b, rows, d), generator=g).to(torch.bfloat16)
+    group = pairs // hkv
+    heads = [h // group for h in range(pairs)]
+    scale = d ** -0.5
+    dk = keys.to(DEV)
+    s = H.score(q.to(DEV), [dk] * pairs, heads, scale, n)
+    ref = O.score_heads([H.f64(q[i]) for i in range(pairs)],
+                        [H.f64(keys[:, heads[i]]) for i in range(pairs)], scale)
+    np.testing.assert_allclose(H.f64(s), ref, rtol=2e-4, atol=1e-7)
+    np.testing.assert_allclose(H.f64(s).sum(axis=1), pairs * rows, rtol=1e-4)
+    assert N.dustin_device_status() == 0
+
+
 @pytest.mark.parametrize("page,d,rows", [(16, 128, 2), (32, 128, 1), (64, 64, 4),
                                           (16, 64, 5), (48, 128, 2), (128, 64, 3)])
 def test_score_heads_paged_matches_contiguous(page, d, rows):

@@ -169,6 +169,24 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(p));
   return p;
 }
+// L2 policy: lines fetched or written under it are the last candidates for
+// eviction (for scratch that is read back soon, then discarded).
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n" : "=l"(p));
+  return p;
+}
+// 8-byte global store under an L2 cache policy.
+__device__ __forceinline__ void st_global_v2_hint(float* p, float a, float b, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v2.f32 [%0], {%1, %2}, %3;\n" ::"l"(p), "f"(a),
+               "f"(b), "l"(policy)
+               : "memory");
+}
+// Drops the 128-byte L2 line at p (128-byte aligned) without writing it
+// back: for scratch that is dead once read.  Its contents become undefined.
+__device__ __forceinline__ void discard_l2_line(const void* p) {
+  asm volatile("discard.global.L2 [%0], 128;\n" ::"l"(p) : "memory");
+}
 // L2 policy: the default eviction priority.
 __device__ __forceinline__ uint64_t policy_evict_normal() {
   uint64_t p;

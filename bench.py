@@ -72,6 +72,9 @@ def parse_args(argv=None):
                    help="approximate CPU work of the oracle leg")
     p.add_argument("--cpu-threads", type=int, default=0,
                    help="oracle threads (0: every core of the affinity mask)")
+    p.add_argument("--profile-once", action="store_true",
+                   help="launch every kernel of the library once on the workload "
+                        "(one target layer), for a profiler's capture")
     p.add_argument("--oracle-worker", action="store_true",
                    help=argparse.SUPPRESS)
     return p.parse_args(argv)
@@ -942,11 +945,92 @@ def run_ours(args):
     return 0
 
 
+def run_profile_once(args):
+    """One launch of every kernel of the library on the workload's shapes
+    (one materialised target layer, so that a capture holds a few GB): target
+    and draft scoring (TMA logits pass + reduce), the selection (clusters),
+    sparse and dense attention of the layer, the sparse call of one sequence
+    (positions split over CTAs: the combine kernel), the multi-layer launch
+    over the layer twice, Quest page statistics and page scores with their
+    page selection (the 256-thread select instance), and the cp.async
+    logits pass (a paged cache with 48-position pages, four sequences)."""
+    import torch
+    from sparse_kv_verification_gb300 import build
+    from sparse_kv_verification_gb300 import inputs as I
+    from sparse_kv_verification_gb300 import native as N
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    build.build()
+    N.load()
+    dev = torch.device("cuda", 0)
+    wl = I.WORKLOADS[args.config]
+    if args.batch:
+        wl = wl.replace(b=args.batch)
+    rep = Replica(wl, dev, 1)
+    inp = rep.inp
+    sync = torch.cuda.synchronize
+    ran = []
+
+    def once(name, fn):
+        fn()
+        sync()
+        ran.append(name)
+
+    once("score target", rep.score_t)
+    once("score draft", rep.score_d)
+    once("select", rep.select)
+    once("sparse attention", rep.attn[0])
+    once("dense attention", rep.full[0])
+    # One sequence: 8 units on 152 SMs, so the positions are split.
+    q1 = inp.q[0][:1].contiguous()
+    k1, v1 = inp.k[0][:1].contiguous(), inp.v[0][:1].contiguous()
+    o1, l1 = torch.empty_like(q1), torch.empty(q1.shape[:3], device=dev)
+    ws1 = N.workspace(N.dustin_sparse_verify_attn_workspace_size(
+        1, wl.hq, wl.hkv, wl.d, wl.w, wl.k), dev)
+    once("sparse attention, one sequence (split + combine)",
+         lambda: N.dustin_sparse_verify_attn(q1, N.kv_desc(k1, v1), wl.hkv, wl.n,
+                                             rep.idx[:1].contiguous(), wl.scale, o1, l1, ws1))
+    kv0 = N.kv_desc(inp.k[0], inp.v[0])
+    o2 = [torch.empty_like(inp.q[0]) for _ in range(2)]
+    l2 = [torch.empty(inp.q[0].shape[:3], device=dev) for _ in range(2)]
+    once("multi-layer sparse attention (the layer twice)",
+         lambda: N.dustin_sparse_verify_attn_layers([inp.q[0], inp.q[0]], [kv0, kv0],
+                                                    wl.hkv, wl.n, rep.idx, wl.scale, o2, l2))
+    page = 16
+    n_pages = (wl.n + page - 1) // page
+    stats = torch.empty((wl.b, wl.hkv, n_pages, 2, wl.d), dtype=torch.bfloat16, device=dev)
+    once("quest page statistics",
+         lambda: N.dustin_quest_page_stats(kv0, wl.b, wl.hkv, wl.d, wl.n, page, stats=stats))
+    q_row = inp.q[0][:, :, 0, :].contiguous()
+    scores = torch.empty((wl.b, wl.hq, n_pages), device=dev)
+    once("quest page scores",
+         lambda: N.dustin_quest_page_scores(q_row, stats, wl.n, page, scores=scores))
+    keep = max(1, wl.k // page)
+    pidx = torch.empty((wl.b * wl.hq, keep), dtype=torch.int32, device=dev)
+    once("quest page selection (short rows)",
+         N.prepare_hybrid_topk(scores.view(wl.b * wl.hq, n_pages), None, keep, 0, 0, 1.0,
+                               -1, N.DUSTIN_NORM_NONE, pidx))
+    bp = min(4, wl.b)
+    pool, _, table = I.to_paged(inp.k_t[0][:bp].contiguous(), None, 48, seed=7)
+    q_p = inp.q_t[:1, :bp].contiguous()
+    s_p = torch.empty((bp, wl.n), device=dev)
+    ws_p = N.workspace(N.dustin_score_heads_workspace_size(bp, wl.n, 1, 1), dev)
+    once("scoring, paged cache of 48-position pages (cp.async logits pass)",
+         lambda: N.dustin_score_heads(q_p, [N.kv_desc(pool, None, table)], inp.kvh_t[:1],
+                                      wl.scale, s_p, ws_p, wl.n))
+    print(json.dumps({"profile_once": ran, "config": workload_config(wl, 1),
+                      "target_pairs_share_kv_heads": len(set(inp.kvh_t)) < len(inp.kvh_t),
+                      "device_status": N.dustin_device_status()}), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.oracle_worker:
         oracle_worker(args)
         return 0
+    if args.profile_once:
+        return run_profile_once(args)
     if args.impl == "reference":
         return run_reference(args)
     if args.sweep:

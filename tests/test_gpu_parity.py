@@ -497,6 +497,36 @@ def test_score_heads_unaligned_output():
     assert torch.isnan(buf[0]) and torch.isnan(buf[1 + b * n:]).all()
 
 
+def test_score_heads_workspace_alignment_and_reuse():
+    """The logits pass keeps its fp32 logits in L2 and the second pass drops
+    them after reading only when n is a multiple of 32 and the workspace
+    starts on a 128-byte boundary.  A workspace that is 16- but not
+    128-byte aligned takes the path that leaves them in memory: the same S
+    bits either way, twice in a row over the same workspaces."""
+    p, b, rows, d, n = 3, 2, 4, 64, 8192
+    g = I.generator(97)
+    q = torch.randn((p, b, rows, d), generator=g).to(torch.bfloat16).to(DEV)
+    keys = [torch.randn((b, 2, n, d), generator=g).to(torch.bfloat16).to(DEV)
+            for _ in range(p)]
+    descs = [N.kv_desc(k) for k in keys]
+    need = N.dustin_score_heads_workspace_size(b, n, p, rows)
+    ws_a = N.workspace(need, DEV)                         # 256-byte aligned
+    raw = torch.empty(need + 256, dtype=torch.uint8, device=DEV)
+    ws_u = raw[16:16 + need]                              # 16-, not 128-byte aligned
+    assert ws_a.data_ptr() % 128 == 0 and ws_u.data_ptr() % 128 == 16
+    outs = []
+    for ws in (ws_a, ws_u, ws_a, ws_u):
+        s = torch.full((b, n), float("nan"), device=DEV)
+        N.dustin_score_heads(q, descs, [0, 1, 1], 0.125, s, ws, n)
+        H.sync()
+        outs.append(s)
+    assert all(torch.equal(outs[0], o) for o in outs[1:])
+    ref = O.score_heads([H.f64(q[i]) for i in range(p)],
+                        [H.f64(keys[i][:, h]) for i, h in enumerate([0, 1, 1])], 0.125)
+    np.testing.assert_allclose(H.f64(outs[0]), ref, rtol=2e-4, atol=1e-7)
+    assert N.dustin_device_status() == 0
+
+
 # ---------------------------------------------------------------- selection
 
 SELECT_CASES = [

@@ -81,7 +81,7 @@ __host__ __device__ constexpr int hist_copies(int threads) {
 struct Shared {
   int warp_vals[kMaxWarps];
   float coef[2];          // fp32 mixing coefficients (alpha mode)
-  int pick[2];
+  int pick[3];            // bucket, keys above it, keys in it
   int xchg[4];            // counts this CTA publishes to its cluster
   double dpart[2];        // this CTA's L1 partial sums (draft, target)
   float4 fbuf[kMaxWarps + 1];
@@ -217,6 +217,11 @@ __device__ void select_mark(cg::cluster_group& cl, int rank, int C, int r,
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t prefix = 0, mask = 0;
   int need = r;
+  // Set when the bucket holding the r-th key holds exactly the keys still
+  // needed: every key whose top bits match is taken, whatever its lower
+  // bits, so the remaining passes and the ranking of equal keys are
+  // skipped (the same set: the order among them no longer matters).
+  bool whole = false;
 #pragma unroll 1
   for (int pass = 0; pass < 3; ++pass) {
     const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
@@ -264,6 +269,7 @@ __device__ void select_mark(cg::cluster_group& cl, int rank, int C, int r,
       if (acc < need && need <= acc + cnt[q]) {
         sh.pick[0] = nb - 1 - tid * bpt - q;
         sh.pick[1] = acc;
+        sh.pick[2] = cnt[q];
       }
       acc += cnt[q];
     }
@@ -271,7 +277,29 @@ __device__ void select_mark(cg::cluster_group& cl, int rank, int C, int r,
     prefix |= (uint32_t)sh.pick[0] << shift;
     mask |= (uint32_t)(nb - 1) << shift;
     need -= sh.pick[1];
+    whole = sh.pick[2] == need;   // the same in every CTA of the cluster
     __syncthreads();
+    if (whole) break;
+  }
+
+  if (whole) {
+    // Take every eligible key whose top bits are at least the prefix.
+    const int w0 = warp * sg.cw, w1 = min(sg.len, w0 + sg.cw);
+    for (int i = w0; i < w0 + sg.cw; i += 32) {
+      const int p = i + lane;
+      bool take = false;
+      if (p < w1) {
+        const int j = sg.lo + p;
+        take = elig(j) && (key(j) & mask) >= prefix;
+      }
+      const unsigned word = __ballot_sync(0xffffffffu, take);
+      if (lane == 0 && word) bits[i >> 5] |= word;
+    }
+    // The other CTAs have read this CTA's histograms before any later round
+    // writes them again.
+    cl.sync();
+    __syncthreads();
+    return;
   }
 
   // Take keys > T, and the first `need` keys == T in position order.

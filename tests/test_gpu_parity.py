@@ -588,6 +588,46 @@ def test_select_ties_across_the_cluster(n):
         np.testing.assert_array_equal(got.cpu().numpy(), want)
 
 
+def _planted(n, top, seed, lo, hi):
+    """Two rows of n scores in [0.25, 0.5) with the values `top` written at
+    random positions in [lo, hi) (the same values, shuffled, in each row)."""
+    g = I.generator(seed)
+    s = 0.25 + 0.25 * torch.rand((2, n), generator=g, dtype=torch.float64)
+    for r in range(2):
+        pos = lo + torch.randperm(hi - lo, generator=g)[: len(top)]
+        s[r, pos] = torch.as_tensor(top, dtype=torch.float64)[torch.randperm(len(top), generator=g)]
+    return s.float()
+
+
+@pytest.mark.parametrize("n", [32768, 3000])
+def test_select_bucket_holds_exactly_the_rest(n):
+    """Scores built so that the bucket holding the budget-th key holds
+    exactly the keys still needed after the first, the second or only the
+    third radix digit (top bits: sign, exponent, 2 mantissa bits; then 11
+    mantissa bits; then the last 10): the set must not depend on where the
+    count first matches, and must equal the oracle's."""
+    ns, nr = 4, 64
+    k = min(2048, n // 4)
+    budget = k - ns - nr
+    # first digit: budget equal values far above the rest
+    a = _planted(n, [4.0] * budget, seed=n + 1, lo=ns, hi=n - nr)
+    # second digit: budget + 68 distinct values sharing the first digit
+    b = _planted(n, [1.0 + i * 2.0 ** -13 for i in range(budget + 68)], seed=n + 2, lo=ns, hi=n - nr)
+    # third digit: pairs that share the first two digits (an odd budget
+    # leaves one key of a pair to the third digit)
+    pairs = [1.0 + ((i // 2) * 1024 + (i % 2)) * 2.0 ** -23 for i in range(2 * budget)]
+    c = _planted(n, pairs, seed=n + 3, lo=ns, hi=n - nr)
+    for sd, kk in ((a, k), (b, k), (c, k), (c, k + 1)):
+        got = H.select(sd.to(DEV), None, kk, ns, nr, 1.0, -1, 0)
+        want = O.hybrid_select(sd.numpy(), None, kk, ns, nr, 1.0, -1, 0)
+        np.testing.assert_array_equal(got.cpu().numpy(), want)
+    # two rounds (draft quota, then target) with the match at different digits
+    for sd, st in ((a, b), (b, c), (c, a)):
+        got = H.select(sd.to(DEV), st.to(DEV), k, ns, nr, 0.5, k // 4 + 1, 1)
+        want = O.hybrid_select(sd.numpy(), st.numpy(), k, ns, nr, 0.5, k // 4 + 1, 1)
+        np.testing.assert_array_equal(got.cpu().numpy(), want)
+
+
 def test_select_single_vector():
     sd = I.synthetic_scores(2, 2000, seed=1)
     got = H.select(sd.to(DEV), None, 100, 4, 4, 1.0, -1, 0)

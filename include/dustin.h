@@ -110,6 +110,17 @@ uint64_t dustin_launch_count(void);
  */
 int dustin_device_status(uint32_t* flags);
 
+/*
+ * Self-test of the bounded wait that every pipeline wait of the library
+ * uses: launches one CTA of 32 threads on `stream` that waits on an
+ * mbarrier no thread ever arrives at, with a limit of `limit_cycles` SM
+ * clock cycles (1 .. 2^31; about 2 * 10^9 inside the compute calls).  The
+ * wait gives up, raises DUSTIN_DEVFLAG_WAIT_TIMEOUT and the kernel returns:
+ * the context stays usable.  Returns DUSTIN_ERR_SHAPE for a limit outside
+ * that range, DUSTIN_ERR_CUDA if the launch fails, DUSTIN_OK otherwise.
+ */
+int dustin_wait_selftest(int64_t limit_cycles, void* stream);
+
 /* ------------------------------------------------------------------------
  * Importance scoring on the scored (layer, head) pairs.
  *

@@ -463,11 +463,55 @@ int dustin_version(void) { return 100; }
 
 uint64_t dustin_launch_count(void) { return g_launches.load(); }
 
+namespace dustin {
+namespace {
+
+__device__ unsigned int g_selftest_flags;
+
+// One warp waits on an mbarrier that expects one arrival nobody makes.
+__global__ void wait_selftest_kernel(long long limit) {
+  __shared__ __align__(8) unsigned long long bar;
+  const uint32_t b = smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  griddep_wait();
+  griddep_launch_dependents();
+  if (!mbar_wait(b, 0, limit) && threadIdx.x == 0)
+    atomicOr(&g_selftest_flags, DUSTIN_DEVFLAG_WAIT_TIMEOUT);
+}
+
+cudaError_t take_selftest_flags(unsigned* flags) {
+  unsigned v = 0, zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_selftest_flags, sizeof(v));
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyToSymbol(g_selftest_flags, &zero, sizeof(zero));
+  *flags |= v;
+  return e;
+}
+
+}  // namespace
+}  // namespace dustin
+
+int dustin_wait_selftest(int64_t limit_cycles, void* stream) {
+  if (limit_cycles < 1 || limit_cycles > (1LL << 31))
+    return fail(DUSTIN_ERR_SHAPE, "dustin_wait_selftest: limit %lld cycles",
+                (long long)limit_cycles);
+  cudaError_t e = launch_pdl(wait_selftest_kernel, dim3(1), dim3(32), 0,
+                             (cudaStream_t)stream, (long long)limit_cycles);
+  if (e != cudaSuccess) return cuda_fail(e, "dustin_wait_selftest");
+  note_launches(1);
+  return DUSTIN_OK;
+}
+
 int dustin_device_status(uint32_t* flags) {
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e, "dustin_device_status");
   unsigned f = 0;
-  if ((e = take_attn_sparse_flags(&f)) != cudaSuccess ||
+  if ((e = take_selftest_flags(&f)) != cudaSuccess ||
+      (e = take_attn_sparse_flags(&f)) != cudaSuccess ||
       (e = take_attn_dense_flags(&f)) != cudaSuccess ||
       (e = take_attn_ml_flags(&f)) != cudaSuccess ||
       (e = take_quest_flags(&f)) != cudaSuccess ||

@@ -22,7 +22,7 @@ DUSTIN_ATTN_KV_READY = 1
 
 EXPORTS = (
     "dustin_status_string", "dustin_last_error", "dustin_version",
-    "dustin_launch_count", "dustin_device_status",
+    "dustin_launch_count", "dustin_device_status", "dustin_wait_selftest",
     "dustin_score_heads_workspace_size", "dustin_score_heads",
     "dustin_score_heads_noalloc", "dustin_score_heads_noalloc_capacity",
     "dustin_hybrid_topk",
@@ -87,6 +87,7 @@ def load(build_if_missing: bool = False, path: Optional[str] = None
         "dustin_version": (I, []),
         "dustin_launch_count": (ctypes.c_uint64, []),
         "dustin_device_status": (I, [P]),
+        "dustin_wait_selftest": (I, [ctypes.c_int64, P]),
         "dustin_score_heads_workspace_size": (S, [I, I, I, I]),
         "dustin_score_heads": (I, [I, I, I, I, I, P, P, P, F, P, P, S, P]),
         "dustin_score_heads_noalloc": (I, [I, I, I, I, I, P, P, P, F, P, P]),
@@ -420,6 +421,12 @@ def dustin_quest_page_scores(q: torch.Tensor, stats: torch.Tensor, n: int,
 
 
 # ------------------------------------------------------------------ misc
+
+def dustin_wait_selftest(limit_cycles: int, stream=None) -> None:
+    """Launches the bounded-wait self-test (one wait that nothing ends)."""
+    _check(load().dustin_wait_selftest(int(limit_cycles),
+                                       _stream(stream, torch.device("cuda"))))
+
 
 def dustin_device_status() -> int:
     """Synchronises the device, returns and clears the device-side flags."""

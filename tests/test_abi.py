@@ -193,3 +193,11 @@ def test_quest_and_window_validation(lib):
     assert wcall(win=None) == 1
     assert wcall(win=kv(stride_n=100)) == 2
     assert wcall(flags=4) == 1
+
+
+def test_wait_selftest_limit_is_checked_before_launch(lib):
+    """The self-test's limit is validated on the host: an out-of-range limit
+    launches nothing (no GPU needed)."""
+    assert lib.dustin_wait_selftest(0, None) == 2
+    assert lib.dustin_wait_selftest(-5, None) == 2
+    assert lib.dustin_wait_selftest((1 << 31) + 1, None) == 2

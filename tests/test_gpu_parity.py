@@ -380,6 +380,23 @@ def test_attention_edge_cases():
     H.assert_attn_close(o, lse, o_ref, l_ref)
 
 
+def test_bounded_wait_gives_up_and_leaves_the_context_usable():
+    """A wait that nothing ends (an mbarrier no thread arrives at), with the
+    bounded wait every pipeline of the library uses: it gives up after its
+    limit, raises the timeout flag, and the next call runs normally."""
+    N.dustin_device_status()                     # clear old flags
+    N.dustin_wait_selftest(2_000_000)            # about a millisecond
+    assert N.dustin_device_status() == 4         # DUSTIN_DEVFLAG_WAIT_TIMEOUT
+    assert N.dustin_device_status() == 0         # read clears
+    q, kk, v = qkv(1, 4, 1, 64, 2, 100, seed=12)
+    idx = torch.tensor([[3, 10, 50]], dtype=torch.int32)
+    o, lse = H.sparse_attn(q.to(DEV), kk.to(DEV), v.to(DEV), idx.to(DEV), 0.2)
+    assert N.dustin_device_status() == 0
+    o_ref, l_ref = O.verify_attention(H.f64(q), H.f64(kk), H.f64(v),
+                                      idx.numpy(), 0.2)
+    H.assert_attn_close(o, lse, o_ref, l_ref)
+
+
 def test_out_of_range_index_is_flagged_not_faulted():
     """The kernel's own bounds check: an index >= n is left out of the
     attention and raises a device flag; no access goes out of bounds."""

@@ -349,7 +349,12 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
       const unsigned vm = __ballot_sync(0xffffffffu, my_off >= 0) &
                           (C::RPW == 32 ? 0xffffffffu : ((1u << C::RPW) - 1u));
       unsigned char* dst = dst_base + s * C::TILE_BYTES + ch * 16;
-#pragma unroll 4
+      // Eight rows' shuffles and copies in flight at once: the producers'
+      // issue rate sets part of the tile period (72B layer back to back:
+      // 27.85 -> 26.65 us against four; sixteen 26.76; the row offset read
+      // from shared memory instead of shuffled 36.0; 32-bit row codes
+      // shuffled and the address formed after 29.1).
+#pragma unroll 8
       for (int it = 0; it < C::RPW / RPI; ++it) {
         const int rr = it * RPI + sub;            // row within this warp's rows
         const long long off = __shfl_sync(0xffffffffu, my_off, rr);

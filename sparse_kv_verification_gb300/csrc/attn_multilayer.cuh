@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(SkCfg<D, MT>::NT, 1)
         const unsigned vm = __ballot_sync(0xffffffffu, my_off >= 0) &
                             (C::RPW == 32 ? 0xffffffffu : ((1u << C::RPW) - 1u));
         unsigned char* dst = dst_base + st * C::TILE_BYTES + ch * 16;
-#pragma unroll 4
+#pragma unroll 8
         for (int q = 0; q < C::RPW / RPI; ++q) {
           const int rr = q * RPI + sub;             // row within this warp's rows
           const long long off = __shfl_sync(0xffffffffu, my_off, rr);

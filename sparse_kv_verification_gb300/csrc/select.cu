@@ -207,7 +207,8 @@ struct Seg {
 
 // Marks the top-r eligible positions of the sequence by key (ties: lower
 // position first) in `bits` (this CTA's segment).  Called by every CTA of
-// the cluster with the same r; xslot is this round's exchange slot.
+// the cluster with the same r; xslot is this call's exchange slot (the
+// m-split makes two calls, draft quota then target).
 template <int THREADS, class KeyF, class EligF>
 __device__ void select_mark(cg::cluster_group& cl, int rank, int C, int r,
                             const Seg& sg, KeyF key, EligF elig,
@@ -295,7 +296,7 @@ __device__ void select_mark(cg::cluster_group& cl, int rank, int C, int r,
       const unsigned word = __ballot_sync(0xffffffffu, take);
       if (lane == 0 && word) bits[i >> 5] |= word;
     }
-    // The other CTAs have read this CTA's histograms before any later round
+    // The other CTAs have read this CTA's histograms before any later call
     // writes them again.
     cl.sync();
     __syncthreads();

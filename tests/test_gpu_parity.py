@@ -645,6 +645,27 @@ def test_select_bucket_holds_exactly_the_rest(n):
         np.testing.assert_array_equal(got.cpu().numpy(), want)
 
 
+def test_select_bucket_holds_exactly_the_rest_short_rows():
+    """The same early stop on the instance for many short rows (one
+    256-thread CTA per row): 320 rows of 2048 scores built so that, over the
+    two budgets, rows stop after the first, the second and the third
+    digit."""
+    rows, n, k = 320, 2048, 128
+    ns, nr = 2, 8
+    budget = k - ns - nr
+    a = _planted(n, [4.0] * budget, seed=71, lo=ns, hi=n - nr)
+    b = _planted(n, [1.0 + i * 2.0 ** -13 for i in range(budget + 40)], seed=72,
+                 lo=ns, hi=n - nr)
+    pairs = [1.0 + ((i // 2) * 1024 + (i % 2)) * 2.0 ** -23 for i in range(2 * budget)]
+    c = _planted(n, pairs, seed=73, lo=ns, hi=n - nr)
+    planted = torch.cat([a, b, c])                      # 6 distinct rows
+    sd = planted[torch.arange(rows) % planted.shape[0]].contiguous()
+    for kk in (k, k + 1):
+        got = H.select(sd.to(DEV), None, kk, ns, nr, 1.0, -1, 0)
+        want = O.hybrid_select(sd.numpy(), None, kk, ns, nr, 1.0, -1, 0)
+        np.testing.assert_array_equal(got.cpu().numpy(), want)
+
+
 def test_select_single_vector():
     sd = I.synthetic_scores(2, 2000, seed=1)
     got = H.select(sd.to(DEV), None, 100, 4, 4, 1.0, -1, 0)

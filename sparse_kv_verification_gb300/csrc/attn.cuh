@@ -419,9 +419,6 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   const int gq = lane >> 2, tq = lane & 3;
 
-  // Window position of rows 16 wm + gq and + 8 (rows past G*w: unused).
-  const int tA = WIN ? (r_lo + wm * 16 + gq) % a.w : 0;
-  const int tB = WIN ? (r_lo + wm * 16 + gq + 8) % a.w : 0;
   for (int t = 0; t < ntot; ++t) {
     const int s = t % C::STAGES;
     if (!mbar_wait(full_bar(s), (t / C::STAGES) & 1, kWaitLimitCycles)) {
@@ -455,6 +452,10 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
     // scale (> 0) is folded into the exponent below, so the maximum is taken
     // on raw scores and converted once per row.
     if (WIN && t == ntiles) {   // the window tile: causal within the window
+      // Window position of rows 16 wm + gq and + 8 (rows past G*w: unused),
+      // formed here so that they hold no registers through the loop.
+      const int tA = (r_lo + wm * 16 + gq) % a.w;
+      const int tB = (r_lo + wm * 16 + gq + 8) % a.w;
 #pragma unroll
       for (int j = 0; j < C::NT8; ++j)
 #pragma unroll
@@ -546,84 +547,196 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
   l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
 
-  // Every issued copy was waited for, so the stages are free to reuse.
-  named_bar_sync(1, C::NCW * 32);
-  if constexpr (C::WN > 1) {
-    float* mb = reinterpret_cast<float*>(sK);
-    constexpr int SLOTS = C::DT * 4 + 4;
-    if (wn > 0) {
-      float* p = mb + ((wn - 1) * MT + wm) * 32 * SLOTS + lane;
-      p[0] = m0;
-      p[32] = m1;
-      p[64] = l0;
-      p[96] = l1;
-#pragma unroll
-      for (int dt = 0; dt < C::DT; ++dt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) p[(4 + dt * 4 + e) * 32] = oacc[dt][e];
-    }
+  if constexpr (C::WN == 4) {
+    // ---- Merge the WN position slices; every consumer warp takes part
+    // (72B layer back to back: 26.56 -> 25.77 us against the merge by the
+    // wn = 0 warps below, which the two-slice instance keeps).
+    // Every warp parks its (m, l) and partial O in shared memory (the stages
+    // are free: every issued copy was waited for); warp (wm, wn) then owns
+    // the d tiles [wn OWN, wn OWN + OWN) of its row tile and folds slices
+    // 1 .. WN-1 into slice 0 in slice order for them, with the pairwise rule
+    //   M' = max(M, m_o),  a = 2^(M - M'),  b = 2^(m_o - M'),
+    //   L' = L a + l_o b,  O' = O a + O_o b
+    // that every warp of the row tile evaluates on the same (m, l) table.
+    // The normalised bf16 rows go through shared memory (the Q rows, no
+    // longer read) so that the global writes are whole 16-byte chunks.
+    constexpr int OWN = C::DT / C::WN;
+    static_assert(MT * C::WN * (C::DT + 1) * 32 * 16 <= 2 * C::STAGES * C::TILE_BYTES,
+                  "slice exchange buffer");
+    const int rA = wm * 16 + gq, rB = rA + 8;
     named_bar_sync(1, C::NCW * 32);
-    if (wn == 0) {
-#pragma unroll 1
-      for (int o = 1; o < C::WN; ++o) {
-        const float* p = mb + ((o - 1) * MT + wm) * 32 * SLOTS + lane;
-        const float om0 = p[0], om1 = p[32], ol0 = p[64], ol1 = p[96];
-        const float M0 = fmaxf(m0, om0), M1 = fmaxf(m1, om1);
-        const float v0 = (M0 == -INFINITY) ? 0.f : M0;
-        const float v1 = (M1 == -INFINITY) ? 0.f : M1;
-        const float a0 = ex2(m0 - v0), b0 = ex2(om0 - v0);
-        const float a1 = ex2(m1 - v1), b1 = ex2(om1 - v1);
-        l0 = l0 * a0 + ol0 * b0;
-        l1 = l1 * a1 + ol1 * b1;
-        m0 = M0;
-        m1 = M1;
-#pragma unroll
-        for (int dt = 0; dt < C::DT; ++dt) {
-          oacc[dt][0] = oacc[dt][0] * a0 + p[(4 + dt * 4 + 0) * 32] * b0;
-          oacc[dt][1] = oacc[dt][1] * a0 + p[(4 + dt * 4 + 1) * 32] * b0;
-          oacc[dt][2] = oacc[dt][2] * a1 + p[(4 + dt * 4 + 2) * 32] * b1;
-          oacc[dt][3] = oacc[dt][3] * a1 + p[(4 + dt * 4 + 3) * 32] * b1;
+    float4* xo = reinterpret_cast<float4*>(sK);                 // [MT][WN][DT][32]
+    float4* xml = xo + MT * C::WN * C::DT * 32;                 // [MT][WN][32]
+    const float4* mine = xo + (wm * C::WN) * C::DT * 32 + lane; // slice 0 of the row tile
+    xml[(wm * C::WN + wn) * 32 + lane] = make_float4(m0, m1, l0, l1);
+  #pragma unroll
+    for (int dt = 0; dt < C::DT; ++dt)
+      xo[((wm * C::WN + wn) * C::DT + dt) * 32 + lane] =
+          make_float4(oacc[dt][0], oacc[dt][1], oacc[dt][2], oacc[dt][3]);
+    named_bar_sync(1, C::NCW * 32);
+    float M0, M1, L0, L1;
+    {
+      const float4 v = xml[(wm * C::WN) * 32 + lane];
+      M0 = v.x;
+      M1 = v.y;
+      L0 = v.z;
+      L1 = v.w;
+    }
+  #pragma unroll
+    for (int dt = 0; dt < C::DT; ++dt) {
+      if (dt / OWN != wn) continue;
+      const float4 v = mine[dt * 32];
+      oacc[dt][0] = v.x;
+      oacc[dt][1] = v.y;
+      oacc[dt][2] = v.z;
+      oacc[dt][3] = v.w;
+    }
+  #pragma unroll 1
+    for (int o = 1; o < C::WN; ++o) {
+      const float4 v = xml[(wm * C::WN + o) * 32 + lane];
+      const float N0 = fmaxf(M0, v.x), N1 = fmaxf(M1, v.y);
+      const float u0 = (N0 == -INFINITY) ? 0.f : N0;
+      const float u1 = (N1 == -INFINITY) ? 0.f : N1;
+      const float a0 = ex2(M0 - u0), b0 = ex2(v.x - u0);
+      const float a1 = ex2(M1 - u1), b1 = ex2(v.y - u1);
+      L0 = __fmaf_rn(L0, a0, __fmul_rn(v.z, b0));
+      L1 = __fmaf_rn(L1, a1, __fmul_rn(v.w, b1));
+      M0 = N0;
+      M1 = N1;
+  #pragma unroll
+      for (int dt = 0; dt < C::DT; ++dt) {
+        if (dt / OWN != wn) continue;
+        const float4 w = mine[(o * C::DT + dt) * 32];
+        oacc[dt][0] = __fmaf_rn(oacc[dt][0], a0, __fmul_rn(w.x, b0));
+        oacc[dt][1] = __fmaf_rn(oacc[dt][1], a0, __fmul_rn(w.y, b0));
+        oacc[dt][2] = __fmaf_rn(oacc[dt][2], a1, __fmul_rn(w.z, b1));
+        oacc[dt][3] = __fmaf_rn(oacc[dt][3], a1, __fmul_rn(w.w, b1));
+      }
+    }
+
+    if (a.splits == 1) {
+      const float i0 = L0 > 0.f ? 1.f / L0 : 0.f;
+      const float i1 = L1 > 0.f ? 1.f / L1 : 0.f;
+  #pragma unroll
+      for (int dt = 0; dt < C::DT; ++dt) {
+        if (dt / OWN != wn) continue;
+        const int col = dt * 8 + 2 * tq;
+        *reinterpret_cast<uint32_t*>(sQ + rA * C::RS + col * 2) =
+            pack_bf16(oacc[dt][0] * i0, oacc[dt][1] * i0);
+        *reinterpret_cast<uint32_t*>(sQ + rB * C::RS + col * 2) =
+            pack_bf16(oacc[dt][2] * i1, oacc[dt][3] * i1);
+      }
+      if (wn == 0 && tq == 0) {
+        const int RA = r_lo + rA, RB = r_lo + rB;
+        if (RA < a.rows)
+          a.lse[row_base + RA] = L0 > 0.f ? (M0 + log2f(L0)) * kLn2 : -INFINITY;
+        if (RB < a.rows)
+          a.lse[row_base + RB] = L1 > 0.f ? (M1 + log2f(L1)) * kLn2 : -INFINITY;
+      }
+      named_bar_sync(1, C::NCW * 32);
+      for (int c = tid; c < C::ROWS * C::CPR; c += C::NCW * 32) {
+        const int r = c / C::CPR, ch = c % C::CPR;
+        if (r_lo + r < a.rows)
+          *reinterpret_cast<uint4*>(a.o + (row_base + r_lo + r) * D + ch * 8) =
+              *reinterpret_cast<const uint4*>(sQ + r * C::RS + ch * 16);
+      }
+    } else {
+      const long long pb = ((long long)blockIdx.x) * C::ROWS;  // (blk, split)
+  #pragma unroll
+      for (int dt = 0; dt < C::DT; ++dt) {
+        if (dt / OWN != wn) continue;
+        const int col = dt * 8 + 2 * tq;
+        *reinterpret_cast<float2*>(a.ws_o + (pb + rA) * D + col) =
+            make_float2(oacc[dt][0], oacc[dt][1]);
+        *reinterpret_cast<float2*>(a.ws_o + (pb + rB) * D + col) =
+            make_float2(oacc[dt][2], oacc[dt][3]);
+      }
+      if (wn == 0 && tq == 0) {
+        a.ws_ml[pb + rA] = make_float2(M0, L0);
+        a.ws_ml[pb + rB] = make_float2(M1, L1);
+      }
+    }
+  } else {
+
+    // Every issued copy was waited for, so the stages are free to reuse.
+    named_bar_sync(1, C::NCW * 32);
+    if constexpr (C::WN > 1) {
+      float* mb = reinterpret_cast<float*>(sK);
+      constexpr int SLOTS = C::DT * 4 + 4;
+      if (wn > 0) {
+        float* p = mb + ((wn - 1) * MT + wm) * 32 * SLOTS + lane;
+        p[0] = m0;
+        p[32] = m1;
+        p[64] = l0;
+        p[96] = l1;
+  #pragma unroll
+        for (int dt = 0; dt < C::DT; ++dt)
+  #pragma unroll
+          for (int e = 0; e < 4; ++e) p[(4 + dt * 4 + e) * 32] = oacc[dt][e];
+      }
+      named_bar_sync(1, C::NCW * 32);
+      if (wn == 0) {
+  #pragma unroll 1
+        for (int o = 1; o < C::WN; ++o) {
+          const float* p = mb + ((o - 1) * MT + wm) * 32 * SLOTS + lane;
+          const float om0 = p[0], om1 = p[32], ol0 = p[64], ol1 = p[96];
+          const float M0 = fmaxf(m0, om0), M1 = fmaxf(m1, om1);
+          const float v0 = (M0 == -INFINITY) ? 0.f : M0;
+          const float v1 = (M1 == -INFINITY) ? 0.f : M1;
+          const float a0 = ex2(m0 - v0), b0 = ex2(om0 - v0);
+          const float a1 = ex2(m1 - v1), b1 = ex2(om1 - v1);
+          l0 = l0 * a0 + ol0 * b0;
+          l1 = l1 * a1 + ol1 * b1;
+          m0 = M0;
+          m1 = M1;
+  #pragma unroll
+          for (int dt = 0; dt < C::DT; ++dt) {
+            oacc[dt][0] = oacc[dt][0] * a0 + p[(4 + dt * 4 + 0) * 32] * b0;
+            oacc[dt][1] = oacc[dt][1] * a0 + p[(4 + dt * 4 + 1) * 32] * b0;
+            oacc[dt][2] = oacc[dt][2] * a1 + p[(4 + dt * 4 + 2) * 32] * b1;
+            oacc[dt][3] = oacc[dt][3] * a1 + p[(4 + dt * 4 + 3) * 32] * b1;
+          }
         }
       }
     }
-  }
-  if (wn != 0) return;
+    if (wn != 0) return;
 
-  // ---- Write: rows r = 16 wm + gq (+8) of this row block.
-  const int rA = wm * 16 + gq, rB = rA + 8;
-  const int RA = r_lo + rA, RB = r_lo + rB;
-  if (a.splits == 1) {
-    const float i0 = l0 > 0.f ? 1.f / l0 : 0.f;
-    const float i1 = l1 > 0.f ? 1.f / l1 : 0.f;
-#pragma unroll
-    for (int dt = 0; dt < C::DT; ++dt) {
-      const int col = dt * 8 + 2 * tq;
-      if (RA < a.rows)
-        *reinterpret_cast<uint32_t*>(a.o + (row_base + RA) * D + col) =
-            pack_bf16(oacc[dt][0] * i0, oacc[dt][1] * i0);
-      if (RB < a.rows)
-        *reinterpret_cast<uint32_t*>(a.o + (row_base + RB) * D + col) =
-            pack_bf16(oacc[dt][2] * i1, oacc[dt][3] * i1);
-    }
-    if (tq == 0) {
-      if (RA < a.rows)
-        a.lse[row_base + RA] = l0 > 0.f ? (m0 + log2f(l0)) * kLn2 : -INFINITY;
-      if (RB < a.rows)
-        a.lse[row_base + RB] = l1 > 0.f ? (m1 + log2f(l1)) * kLn2 : -INFINITY;
-    }
-  } else {
-    const long long pb = ((long long)blockIdx.x) * C::ROWS;  // (blk, split)
-#pragma unroll
-    for (int dt = 0; dt < C::DT; ++dt) {
-      const int col = dt * 8 + 2 * tq;
-      *reinterpret_cast<float2*>(a.ws_o + (pb + rA) * D + col) =
-          make_float2(oacc[dt][0], oacc[dt][1]);
-      *reinterpret_cast<float2*>(a.ws_o + (pb + rB) * D + col) =
-          make_float2(oacc[dt][2], oacc[dt][3]);
-    }
-    if (tq == 0) {
-      a.ws_ml[pb + rA] = make_float2(m0, l0);
-      a.ws_ml[pb + rB] = make_float2(m1, l1);
+    // ---- Write: rows r = 16 wm + gq (+8) of this row block.
+    const int rA = wm * 16 + gq, rB = rA + 8;
+    const int RA = r_lo + rA, RB = r_lo + rB;
+    if (a.splits == 1) {
+      const float i0 = l0 > 0.f ? 1.f / l0 : 0.f;
+      const float i1 = l1 > 0.f ? 1.f / l1 : 0.f;
+  #pragma unroll
+      for (int dt = 0; dt < C::DT; ++dt) {
+        const int col = dt * 8 + 2 * tq;
+        if (RA < a.rows)
+          *reinterpret_cast<uint32_t*>(a.o + (row_base + RA) * D + col) =
+              pack_bf16(oacc[dt][0] * i0, oacc[dt][1] * i0);
+        if (RB < a.rows)
+          *reinterpret_cast<uint32_t*>(a.o + (row_base + RB) * D + col) =
+              pack_bf16(oacc[dt][2] * i1, oacc[dt][3] * i1);
+      }
+      if (tq == 0) {
+        if (RA < a.rows)
+          a.lse[row_base + RA] = l0 > 0.f ? (m0 + log2f(l0)) * kLn2 : -INFINITY;
+        if (RB < a.rows)
+          a.lse[row_base + RB] = l1 > 0.f ? (m1 + log2f(l1)) * kLn2 : -INFINITY;
+      }
+    } else {
+      const long long pb = ((long long)blockIdx.x) * C::ROWS;  // (blk, split)
+  #pragma unroll
+      for (int dt = 0; dt < C::DT; ++dt) {
+        const int col = dt * 8 + 2 * tq;
+        *reinterpret_cast<float2*>(a.ws_o + (pb + rA) * D + col) =
+            make_float2(oacc[dt][0], oacc[dt][1]);
+        *reinterpret_cast<float2*>(a.ws_o + (pb + rB) * D + col) =
+            make_float2(oacc[dt][2], oacc[dt][3]);
+      }
+      if (tq == 0) {
+        a.ws_ml[pb + rA] = make_float2(m0, l0);
+        a.ws_ml[pb + rB] = make_float2(m1, l1);
+      }
     }
   }
 }

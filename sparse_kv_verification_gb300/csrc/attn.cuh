@@ -569,7 +569,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
     float4* xml = xo + MT * C::WN * C::DT * 32;                 // [MT][WN][32]
     const float4* mine = xo + (wm * C::WN) * C::DT * 32 + lane; // slice 0 of the row tile
     xml[(wm * C::WN + wn) * 32 + lane] = make_float4(m0, m1, l0, l1);
-  #pragma unroll
+#pragma unroll
     for (int dt = 0; dt < C::DT; ++dt)
       xo[((wm * C::WN + wn) * C::DT + dt) * 32 + lane] =
           make_float4(oacc[dt][0], oacc[dt][1], oacc[dt][2], oacc[dt][3]);
@@ -582,7 +582,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
       L0 = v.z;
       L1 = v.w;
     }
-  #pragma unroll
+#pragma unroll
     for (int dt = 0; dt < C::DT; ++dt) {
       if (dt / OWN != wn) continue;
       const float4 v = mine[dt * 32];
@@ -591,7 +591,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
       oacc[dt][2] = v.z;
       oacc[dt][3] = v.w;
     }
-  #pragma unroll 1
+#pragma unroll 1
     for (int o = 1; o < C::WN; ++o) {
       const float4 v = xml[(wm * C::WN + o) * 32 + lane];
       const float N0 = fmaxf(M0, v.x), N1 = fmaxf(M1, v.y);
@@ -603,7 +603,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
       L1 = __fmaf_rn(L1, a1, __fmul_rn(v.w, b1));
       M0 = N0;
       M1 = N1;
-  #pragma unroll
+#pragma unroll
       for (int dt = 0; dt < C::DT; ++dt) {
         if (dt / OWN != wn) continue;
         const float4 w = mine[(o * C::DT + dt) * 32];
@@ -617,7 +617,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
     if (a.splits == 1) {
       const float i0 = L0 > 0.f ? 1.f / L0 : 0.f;
       const float i1 = L1 > 0.f ? 1.f / L1 : 0.f;
-  #pragma unroll
+#pragma unroll
       for (int dt = 0; dt < C::DT; ++dt) {
         if (dt / OWN != wn) continue;
         const int col = dt * 8 + 2 * tq;
@@ -642,7 +642,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
       }
     } else {
       const long long pb = ((long long)blockIdx.x) * C::ROWS;  // (blk, split)
-  #pragma unroll
+#pragma unroll
       for (int dt = 0; dt < C::DT; ++dt) {
         if (dt / OWN != wn) continue;
         const int col = dt * 8 + 2 * tq;
@@ -669,14 +669,14 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
         p[32] = m1;
         p[64] = l0;
         p[96] = l1;
-  #pragma unroll
+#pragma unroll
         for (int dt = 0; dt < C::DT; ++dt)
-  #pragma unroll
+#pragma unroll
           for (int e = 0; e < 4; ++e) p[(4 + dt * 4 + e) * 32] = oacc[dt][e];
       }
       named_bar_sync(1, C::NCW * 32);
       if (wn == 0) {
-  #pragma unroll 1
+#pragma unroll 1
         for (int o = 1; o < C::WN; ++o) {
           const float* p = mb + ((o - 1) * MT + wm) * 32 * SLOTS + lane;
           const float om0 = p[0], om1 = p[32], ol0 = p[64], ol1 = p[96];
@@ -689,7 +689,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
           l1 = l1 * a1 + ol1 * b1;
           m0 = M0;
           m1 = M1;
-  #pragma unroll
+#pragma unroll
           for (int dt = 0; dt < C::DT; ++dt) {
             oacc[dt][0] = oacc[dt][0] * a0 + p[(4 + dt * 4 + 0) * 32] * b0;
             oacc[dt][1] = oacc[dt][1] * a0 + p[(4 + dt * 4 + 1) * 32] * b0;
@@ -707,7 +707,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
     if (a.splits == 1) {
       const float i0 = l0 > 0.f ? 1.f / l0 : 0.f;
       const float i1 = l1 > 0.f ? 1.f / l1 : 0.f;
-  #pragma unroll
+#pragma unroll
       for (int dt = 0; dt < C::DT; ++dt) {
         const int col = dt * 8 + 2 * tq;
         if (RA < a.rows)
@@ -725,7 +725,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
       }
     } else {
       const long long pb = ((long long)blockIdx.x) * C::ROWS;  // (blk, split)
-  #pragma unroll
+#pragma unroll
       for (int dt = 0; dt < C::DT; ++dt) {
         const int col = dt * 8 + 2 * tq;
         *reinterpret_cast<float2*>(a.ws_o + (pb + rA) * D + col) =

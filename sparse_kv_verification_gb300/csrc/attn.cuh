@@ -657,7 +657,6 @@ __global__ void __launch_bounds__(AttnCfg<D, MT>::NT, 1)
       }
     }
   } else {
-
     // Every issued copy was waited for, so the stages are free to reuse.
     named_bar_sync(1, C::NCW * 32);
     if constexpr (C::WN > 1) {
